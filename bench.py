@@ -1,0 +1,386 @@
+#!/usr/bin/env python3
+"""Benchmark of the per-layer mixed-precision AdamW step on GB300.
+
+Workload (default): one h=2560 decoder layer (100,930,560 parameters), R = 4
+BF16 gradient replicas averaged in the kernel, global grad-norm clip at 1.0,
+lr 1e-5, betas 0.9/0.999, eps 1e-8, weight decay 0.01.  A step is one
+slide_layer_step: the clip pre-pass plus the fused
+grad_reduce_adamw_cast kernel over one batch of R synthetic replicas (four
+pre-generated batches are cycled; every step touches ~4.2 GB, far more than
+the 129 MB L2).  The warm-up steps play the workload's pre-warm of m and v.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank updates its own
+layer (independent problems, no collective on the data path: weak scaling);
+the value is all ranks' parameters over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "LayerAdam Gparam/s & HBM GB/s vs ~8 TB/s; host-streamed s/step vs link BW"
+UNIT = "Gparam/s"
+N_BATCHES = 4
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3],
+                    help="HBM-resident workload (1: h2560 R1, 2: h2560 R4 clip, 3: h5120 R8)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--soak-s", type=float, default=1.5,
+                    help="seconds of untimed steps before the timed region (clocks settle, samples)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    return args
+
+
+# ---------------------------------------------------------------- env ----
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sms, maxs, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sms.append(float(parts[1]))
+                    maxs.append(float(parts[2]))
+                except ValueError:
+                    continue
+                n += 1
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sms) if sms else None,
+                "sm_max_mhz": max(maxs) if maxs else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+def workload(cfg):
+    from synth import workloads as W
+    return W.ALL[cfg]()
+
+
+# ------------------------------------------------------------ oracle ----
+
+def oracle_sample_rate(w, n_sample, steps_budget_s, max_steps, seed_offset=0):
+    """Time the oracle (single thread, as it stands) on a contiguous slice of
+    the workload's unit treated as a layer of its own (the clip, when on,
+    is over the slice).  Inputs are generated before each timed call."""
+    import numpy as np
+    import oracle
+    import synth
+
+    sp = synth.spec(w.seed, w.grad_kind, w.zero_prob)
+    hp = oracle.hparams(*w.hparams_tuple())
+    th = synth.master(n_sample, w.seed)
+    m, v = np.zeros(n_sample, np.float32), np.zeros(n_sample, np.float32)
+    wb = np.zeros(n_sample, np.uint16)
+    scale = w.tensor_scales(0)[0]
+    batches = [[synth.grad(n_sample, sp, 0, b + 1 + seed_offset, r, scale) for r in range(w.R)]
+               for b in range(2)]
+    elapsed, steps = 0.0, 0
+    # a time budget > 0 stops early once spent (at least 2 steps); 0 runs max_steps
+    while steps < max_steps and (steps_budget_s <= 0 or elapsed < steps_budget_s or steps < 2):
+        g = batches[steps % 2]
+        t0 = time.perf_counter()
+        oracle.layer_step(g, th, m, v, wb, hp, steps + 1)
+        elapsed += time.perf_counter() - t0
+        steps += 1
+    return n_sample * steps / elapsed / 1e9, steps, elapsed
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = workload(args.config)
+    # calibrate, then size each step's sample so the whole run takes ~2 minutes
+    rate, _, _ = oracle_sample_rate(w, 1 << 20, 0.5, 3, seed_offset=1000)
+    per_step_s = 120.0 / (args.steps + args.warmup)
+    n_s = int(rate * 1e9 * per_step_s) // 4096 * 4096
+    n_s = max(4096, min(n_s, w.units[0].numel, 1 << 24))
+    oracle_sample_rate(w, n_s, 0.0, args.warmup, seed_offset=2000)  # untimed warm-up
+    value, steps, elapsed = oracle_sample_rate(w, n_s, 0.0, args.steps)
+    sample = (f"first {n_s} parameters of the {w.name} unit treated as a layer of their own "
+              f"(R={w.R}{', clip over the sample' if w.max_grad_norm > 0 else ''}), "
+              f"{steps} steps; inputs generated outside the timed calls")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * elapsed / steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description, "params_per_step": n_s},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------- ours ----
+
+def run_ours(args):
+    import torch
+
+    import mixed_precision_adam_grad_gb300 as S
+    import synth
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    w = workload(args.config)
+    n = w.units[0].numel
+    R = w.R
+    clip = w.max_grad_norm > 0
+    hp = S.hparams(*w.hparams_tuple())
+    stream = torch.cuda.Stream()
+
+    st = S.slide_state_create([n], R, device=local)
+    try:
+        th_d = S.slide_layer_ptrs(st, 0)[0]
+        synth.dev_master(th_d, n, w.seed + 100 * rank, stream=stream.cuda_stream)
+        batches = []
+        for b in range(N_BATCHES):
+            reps = [torch.empty(n + 64, dtype=torch.int16, device="cuda") for _ in range(R)]
+            for r, t in enumerate(reps):
+                for (off, ln), sc in zip(w.units[0].segments(), w.tensor_scales(0)):
+                    synth.dev_grad(t.data_ptr() + 2 * off, ln, synth.spec(w.seed + 100 * rank, w.grad_kind,
+                                                                          w.zero_prob),
+                                   0, b + 1, r, sc, offset=off, stream=stream.cuda_stream)
+            batches.append(reps)
+        torch.cuda.synchronize()
+
+        def step(i):
+            S.slide_layer_step(st, 0, batches[i % N_BATCHES], hp, stream)
+
+        for i in range(args.warmup):
+            step(i)
+        torch.cuda.synchronize()
+
+        gpu_index = local
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        if vis:
+            try:
+                gpu_index = int(vis.split(",")[local])
+            except ValueError:
+                pass
+        sampler = ClockSampler(gpu_index)
+        sampler.start()
+        # soak: same steps, untimed, so clocks settle and the sampler sees load
+        t_end = time.time() + args.soak_s
+        i = 0
+        while time.time() < t_end:
+            for _ in range(20):
+                step(i)
+                i += 1
+            stream.synchronize()
+
+        K = args.steps
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+        for trio in ev:          # create the CUDA events (torch creates them on first record)
+            for e in trio:
+                e.record(stream)
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for k in range(K):
+            S.slide_trace_events(st, ev[k][0], ev[k][1], ev[k][2])
+            step(k)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        clocks = sampler.stop()
+        S.slide_trace_events(st)
+        ms_total = start.elapsed_time(stop)
+        pre_ms = [e[0].elapsed_time(e[1]) for e in ev]
+        upd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+        if dist:
+            t = torch.tensor([ms_total], device="cuda", dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms_total = float(t.item())
+
+        # end to end through the public API: pinned host replicas in, BF16 copy out
+        e2e = None
+        if not args.no_e2e:
+            Ke = max(3, min(args.e2e_steps, K))
+            host_reps = [torch.empty(n, dtype=torch.int16, pin_memory=True) for _ in range(R)]
+            for r in range(R):
+                host_reps[r].copy_(batches[0][r][:n])
+            dev_reps = [torch.empty(n + 64, dtype=torch.int16, device="cuda") for _ in range(R)]
+            out_dev = torch.empty(n + 64, dtype=torch.int16, device="cuda")
+            out_host = torch.empty(n, dtype=torch.int16, pin_memory=True)
+            torch.cuda.synchronize()
+
+            def e2e_step():
+                with torch.cuda.stream(stream):
+                    for r in range(R):
+                        dev_reps[r][:n].copy_(host_reps[r], non_blocking=True)
+                    S.slide_layer_step(st, 0, dev_reps, hp, stream, out_dev)
+                    out_host.copy_(out_dev[:n], non_blocking=True)
+
+            for _ in range(3):
+                e2e_step()
+            torch.cuda.synchronize()
+            if dist:
+                dist.barrier()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(Ke):
+                e2e_step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms_e2e = e0.elapsed_time(e1)
+            if dist:
+                t = torch.tensor([ms_e2e], device="cuda", dtype=torch.float64)
+                dist.all_reduce(t, op=dist.ReduceOp.MAX)
+                ms_e2e = float(t.item())
+            e2e = {"value": n * Ke * world / (ms_e2e * 1e-3) / 1e9, "unit": UNIT,
+                   "h2d_bytes_per_step": 2 * R * n, "d2h_bytes_per_step": 2 * n, "steps": Ke}
+    finally:
+        S.slide_state_destroy(st)
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_kind = measured_peaks()
+    bytes_upd = (26 + 2 * R) * n
+    bytes_pre = 2 * R * n if clip else 0
+    upd_avg = statistics.mean(upd_ms)
+    pre_avg = statistics.mean(pre_ms) if clip else 0.0
+    ach_upd = bytes_upd / (upd_avg * 1e-3) / 1e9
+    ach_pre = bytes_pre / (pre_avg * 1e-3) / 1e9 if clip else None
+    ms_step = ms_total / K
+    value = n * K * world / (ms_total * 1e-3) / 1e9
+    step_bytes = bytes_upd + bytes_pre
+
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        rate, steps, el = oracle_sample_rate(w, 1 << 24 if n >= (1 << 24) else n, 12.0, 1000)
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"first {min(n, 1 << 24)} parameters of the layer as a layer of their own, "
+                         f"R={R}{', clip over the sample' if clip else ''}, {steps} steps "
+                         f"({el:.1f} s of single-thread CPU time; inputs generated outside the timed calls)"}
+    traffic = None
+    prof = os.path.join(ROOT, "profiles", f"traffic_{w.name}.json")
+    if os.path.exists(prof):
+        with open(prof) as f:
+            traffic = json.load(f).get("grad_reduce_adamw_cast_bytes_per_launch")
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description, "params": n, "replicas": R,
+                   "max_grad_norm": w.max_grad_norm, "parallelism": f"replicas-only x{world}",
+                   "l2": f"inputs larger than L2: each step touches {step_bytes / 1e9:.2f} GB; "
+                         f"{N_BATCHES} gradient batches cycled",
+                   "clock_samples": "nvidia-smi every 200 ms over a soak of the same step and the "
+                                    "timed region"},
+        "hbm_gbs": step_bytes / (ms_step * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "kernel": "grad_reduce_adamw_cast",
+                     "achieved": ach_upd, "peak": peak, "unit": "GB/s", "frac": ach_upd / peak,
+                     "traffic": traffic, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                     "bytes_per_launch": bytes_upd, "avg_launch_ms": upd_avg,
+                     "bytes_per_param": 26 + 2 * R},
+        "prepass": ({"kernel": "grad_sqnorm", "achieved": ach_pre, "unit": "GB/s", "frac": ach_pre / peak,
+                     "bytes_per_launch": bytes_pre, "avg_launch_ms": pre_avg} if clip else None),
+        "step_roofline_frac": (step_bytes / (ms_step * 1e-3) / 1e9) / peak,
+        "gpu_launches": K * (2 if clip else 1),
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

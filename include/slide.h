@@ -1,0 +1,216 @@
+/*
+ * slide.h — C ABI of the GB300-native per-layer mixed-precision optimizer step
+ * of host-resident layer-streaming fine-tuning.
+ *
+ * What the step computes (the pages print no update equation; the reading is
+ * stated here once and used by every entry point):
+ *   for each parameter i of layer l, with R gradient replicas g_r (BF16) and
+ *   the layer's own 1-based update count t:
+ *     g   = (sum_r g_r[i], in FP32, replica order) / R       -- replica mean
+ *     g  *= min(1, c / (||g||_2 + 1e-6))   if c = max_grad_norm > 0,
+ *           the norm taken over the whole layer's mean gradient
+ *     m   = beta1*m + (1-beta1)*g
+ *     v   = beta2*v + (1-beta2)*g*g
+ *     th  = th*(1 - lr*wd)                                    -- decoupled decay
+ *     th  = th - (lr/(1-beta1^t)) * m / (sqrt(v)/sqrt(1-beta2^t) + eps)
+ *     w   = bf16_round_nearest_even(th)                        -- compute copy
+ *   th, m, v are FP32 and updated in place; w is the BF16 compute copy.
+ *   Each line is one FP32 operation (no contraction); the scalars
+ *   1-beta, 1-lr*wd, lr/(1-beta1^t), sqrt(1-beta2^t) are formed in double from
+ *   the FP32 hyper-parameters and rounded once to FP32.
+ *
+ * Sources (page title, section):
+ *   - "SlideDP: Scaling Host-Resident LLM Fine-Tuning Across Multiple GPUs":
+ *     Prerequisites (mixed-precision Adam keeps 16N bytes: BF16 weights and
+ *     gradients 2N + 2N, FP32 master 4N, FP32 Adam moments 8N); Core method
+ *     (one authoritative FP32 master and Adam moments (m_l, v_l) per layer,
+ *     updated once per iteration by LayerAdam; gradients reduced on the GPU
+ *     before they leave it; a bounded, reusable BF16 layer window per GPU);
+ *     Method steps (the chain backward -> reduce -> transfer -> Adam per layer,
+ *     and the version gate: the next delivery of a layer waits for its update).
+ *   - "An Efficient Heterogeneous Co-Design for Fine-Tuning on a Single GPU"
+ *     (SlideFormer), sections 2.1-2.2: layer-granular sliding window with
+ *     prefetch of the next layer and asynchronous update, a pre-allocated
+ *     fixed-size GPU window, FP32 -> BF16 conversion of updated weights.
+ *   - "Accelerating the Training of Large Language Models using Efficient
+ *     Activation Rematerialization and Optimal Hybrid Parallelism", section 3
+ *     (12 = 4 + 4 + 4 bytes of FP32 master and Adam states per parameter) and
+ *     section 5.1 (event-serialised copies, ping-pong buffers, pinned memory).
+ *
+ * Conventions for every function:
+ *   - Return a slide_status; nothing throws across the ABI.  On an error the
+ *     call enqueues nothing and changes no state (except SLIDE_ERR_ABORTED,
+ *     below), and slide_last_error() describes it.
+ *   - "device pointer" = address in the GPU's memory (cudaMalloc or a
+ *     PyTorch CUDA tensor); "host pointer" = ordinary or pinned CPU memory.
+ *   - Device pointers must be 16-byte aligned; lengths are arbitrary.
+ *   - A slide_state is not thread-safe: use one from one host thread at a time.
+ *   - Streams are cudaStream_t values (NULL = the legacy default stream).
+ */
+#ifndef SLIDE_H
+#define SLIDE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Exported entry points; everything else in the library is hidden. */
+#if defined(__GNUC__)
+#define SLIDE_API __attribute__((visibility("default")))
+#else
+#define SLIDE_API
+#endif
+
+/* Same type as cudaStream_t, declared without the CUDA headers. */
+typedef struct CUstream_st *slide_stream_t;
+
+#define SLIDE_ABI_VERSION 1
+#define SLIDE_MAX_REPLICAS 8
+
+typedef enum {
+    SLIDE_OK = 0,
+    SLIDE_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or hyper-parameter */
+    SLIDE_ERR_OOM_DEVICE = 2,  /* a device allocation failed (all partial ones freed) */
+    SLIDE_ERR_OOM_HOST = 3,    /* a pinned host allocation failed (all partial ones freed) */
+    SLIDE_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+    SLIDE_ERR_VERSION = 5,     /* the same-version invariant would be broken */
+    SLIDE_ERR_TIMEOUT = 6,     /* a bounded host wait ran out (timeout_ms) */
+    SLIDE_ERR_NONFINITE = 7,   /* SLIDE_FLAG_CHECK_FINITE saw a NaN/Inf gradient */
+    SLIDE_ERR_ABORTED = 8,     /* a streamed sweep stopped part-way; see slide_model_step_streamed */
+    SLIDE_ERR_STATE = 9        /* call does not fit the state's residency */
+} slide_status;
+
+enum {
+    SLIDE_RESIDENCY_HBM = 0,          /* master, m, v and the BF16 copy live in HBM */
+    SLIDE_RESIDENCY_HOST_STREAMED = 1 /* they live in pinned host memory; a 2-slot HBM window */
+};
+
+enum {
+    SLIDE_FLAG_CHECK_FINITE = 1u      /* check the mean gradient for NaN/Inf each step */
+};
+
+/* Adam hyper-parameters (FP32).  Valid: lr >= 0, 0 <= beta1 < 1,
+ * 0 <= beta2 < 1, eps >= 0, weight_decay >= 0, all finite;
+ * max_grad_norm <= 0 turns the global clip off. */
+typedef struct {
+    float lr, beta1, beta2, eps, weight_decay, max_grad_norm;
+} slide_adam_hparams;
+
+/* State description.  layer_numel is read during slide_state_create only. */
+typedef struct {
+    int32_t n_layers;            /* >= 1 units (decoder layers, embedding, head ...) */
+    const int64_t *layer_numel;  /* host array [n_layers]; each >= 0 parameters */
+    int32_t n_replicas;          /* R, 1..SLIDE_MAX_REPLICAS */
+    int32_t residency;           /* SLIDE_RESIDENCY_* */
+    int32_t window_layers;       /* streamed: must be 2 (0 = 2) */
+    int32_t device;              /* CUDA device ordinal */
+    uint32_t timeout_ms;         /* streamed: bound of each host wait (0 = 600000) */
+    uint32_t flags;              /* SLIDE_FLAG_* */
+    int64_t chunk_bytes;         /* streamed: copy chunk (0 = 64 MiB); multiple of 256 */
+} slide_config;
+
+typedef struct slide_state slide_state; /* opaque; owns all of its memory */
+
+/* Gradient callback of the streamed step (stands in for a layer's backward):
+ * fill the R BF16 replica buffers of unit `layer` (device pointers, each
+ * layer_numel[layer] elements, owned by the state) with work enqueued on
+ * `stream`.  Return 0 on success; any other value aborts the sweep. */
+typedef int (*slide_grad_fn)(void *user, int32_t layer, void *const *replica_dev_ptrs,
+                             slide_stream_t stream);
+
+/* Create a state: allocates master, m, v, the BF16 copy (all zero, t = 0) and
+ * the per-layer device scratch of the clip reduction; for the streamed
+ * residency also the pinned host state, the 2-slot HBM window and the copy
+ * and compute streams.  *out is set only on SLIDE_OK. */
+SLIDE_API slide_status slide_state_create(const slide_config *cfg, slide_state **out);
+
+/* Free everything the state owns after waiting for its own streams.
+ * NULL-safe.  Work the caller enqueued on its own streams must be done. */
+SLIDE_API void slide_state_destroy(slide_state *st);
+
+/* Bytes slide_state_create would allocate for cfg, computed on the host
+ * without touching a GPU: device (HBM) bytes and pinned host bytes. */
+SLIDE_API slide_status slide_state_bytes(const slide_config *cfg, int64_t *device_bytes,
+                               int64_t *host_pinned_bytes);
+
+/* One optimizer step of one layer (HBM residency): enqueue on `stream` the
+ * clip pre-pass (if max_grad_norm > 0) and the fused kernel
+ * grad_reduce_adamw_cast for step t = t_layer + 1, then set t_layer = t.
+ *   grad_replicas: host array of R device pointers, each to layer_numel[layer]
+ *     BF16 values, 16-byte aligned; caller-owned, read-only, and must stay
+ *     valid until the enqueued work has run.
+ *   bf16_out: device pointer receiving the BF16 copy, or NULL for the state's
+ *     own copy (slide_layer_ptrs).  16-byte aligned.
+ * Stream-ordered: returns before the GPU finishes.  Steps of one layer must be
+ * ordered with each other (same stream, or synchronised by the caller). */
+SLIDE_API slide_status slide_layer_step(slide_state *st, int32_t layer, const void *const *grad_replicas,
+                              const slide_adam_hparams *hp, slide_stream_t stream, void *bf16_out);
+
+/* One synchronous step of every unit of a host-streamed state (residency
+ * SLIDE_RESIDENCY_HOST_STREAMED).  Requires every unit's t to be equal on
+ * entry (same version) else SLIDE_ERR_VERSION.
+ *   forward sweep, l = 0..L-1: the BF16 copy of unit l is copied host->device
+ *     into window slot l%2 (the delivery of the weights a forward would use);
+ *   reverse sweep, l = L-1..0: master/m/v of l are copied host->device into
+ *     its slot, fn(user, l, replicas, compute stream) produces the R gradient
+ *     replicas in the slot, the fused step updates l, and master/m/v and the
+ *     new BF16 copy are copied device->host; the copy of l-1 into the other
+ *     slot overlaps the update of l and the write-back of l+1, handing the
+ *     slot over chunk by chunk.
+ * Each unit is updated exactly once; every t becomes t+1.  Returns after the
+ * last write-back is complete.  If fn fails or a wait times out the sweep
+ * stops: units already written back carry t+1, the rest t, the state is marked
+ * aborted and every later step returns SLIDE_ERR_ABORTED until slide_layer_set
+ * has restored a common version on all units. */
+SLIDE_API slide_status slide_model_step_streamed(slide_state *st, slide_grad_fn fn, void *user,
+                                       const slide_adam_hparams *hp);
+
+/* Copy host arrays into a layer's master / m / v (any may be NULL: left
+ * unchanged) and set its step count t (>= 0).  Also rewrites the BF16 copy as
+ * bf16(master) when master is given.  Synchronous.  Clears the aborted mark
+ * once all units share one t. */
+SLIDE_API slide_status slide_layer_set(slide_state *st, int32_t layer, const float *master, const float *m,
+                             const float *v, int64_t step);
+
+/* Copy a layer's master / m / v / BF16 copy into host arrays (any may be NULL)
+ * and report t.  Synchronous: waits for the state's and the device's work. */
+SLIDE_API slide_status slide_layer_get(slide_state *st, int32_t layer, float *master, float *m, float *v,
+                             uint16_t *bf16, int64_t *step);
+
+/* Where a layer's arrays live: device pointers for the HBM residency, pinned
+ * host pointers for the streamed one (owned by the state; valid until destroy). */
+SLIDE_API slide_status slide_layer_ptrs(slide_state *st, int32_t layer, float **master, float **m, float **v,
+                              uint16_t **bf16);
+
+/* Clip coefficient used by the last slide_layer_step of `layer` that had the
+ * clip on (copied from the device; synchronous).  1.0 before any such step. */
+SLIDE_API slide_status slide_layer_last_clip_coef(slide_state *st, int32_t layer, float *coef);
+
+/* Non-finite check (SLIDE_FLAG_CHECK_FINITE): waits for the device, then
+ * returns SLIDE_ERR_NONFINITE if a step of `layer` since the previous call saw
+ * a NaN or Inf in its mean gradient (and clears that mark), else SLIDE_OK.
+ * Without the flag it always returns SLIDE_OK.  The update itself is not
+ * skipped: the caller decides what to do (for example restore with
+ * slide_layer_set). */
+SLIDE_API slide_status slide_layer_status(slide_state *st, int32_t layer);
+
+/* Tracing: CUDA events (cudaEvent_t values, created by the caller) that every
+ * following slide_layer_step of this state records on its stream: before the
+ * clip pre-pass, before the fused kernel and after it (any may be NULL; all
+ * NULL turns tracing off).  Recording adds no synchronisation.  The caller may
+ * pass fresh events before each step to time every launch separately. */
+SLIDE_API slide_status slide_trace_events(slide_state *st, void *ev_prepass_start,
+                                          void *ev_update_start, void *ev_update_stop);
+
+/* Message of the last error on this host thread ("" if none). */
+SLIDE_API const char *slide_last_error(void);
+
+/* SLIDE_ABI_VERSION of the loaded library. */
+SLIDE_API int32_t slide_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

@@ -1,0 +1,520 @@
+// slide_api.cu — the C ABI declared in include/slide.h: argument checks,
+// status codes, the thread-local last error, state allocation and the
+// HBM-resident layer step.  The streamed residency's sweep is in
+// stream_engine.cu.
+//
+// The state layout follows the 16N accounting of "SlideDP: Scaling
+// Host-Resident LLM Fine-Tuning Across Multiple GPUs" (Prerequisites): per
+// parameter 4 bytes of FP32 master, 4 + 4 of FP32 Adam moments and 2 of the
+// BF16 compute copy owned by the state (the 2 bytes of BF16 gradient per
+// replica are the caller's).  Every array starts on a 256-byte boundary of
+// one arena allocation, allocated once at creation (no allocation on the
+// step path).
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "slide.h"
+#include "slide_kernels.h"
+#include "slide_state.h"
+
+namespace slide {
+
+static thread_local std::string g_last_error;
+
+slide_status fail(slide_status code, const std::string &msg)
+{
+    g_last_error = msg;
+    return code;
+}
+
+slide_status fail_cuda(cudaError_t e, const char *what)
+{
+    std::string msg = std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")";
+    g_last_error = msg;
+    if (e == cudaErrorMemoryAllocation)
+        return SLIDE_ERR_OOM_DEVICE;
+    return SLIDE_ERR_CUDA;
+}
+
+void clear_error() { g_last_error.clear(); }
+
+// Bias corrections of update t (1-based): bc1 = 1 - beta1^t, bc2 = 1 - beta2^t,
+// formed in double from the FP32 hyper-parameters; each scalar rounded once.
+AdamScalars adam_scalars_for(const slide_adam_hparams &hp, int64_t t)
+{
+    const double b1 = hp.beta1, b2 = hp.beta2;
+    const double bc1 = 1.0 - std::pow(b1, (double)t);
+    const double bc2 = 1.0 - std::pow(b2, (double)t);
+    AdamScalars s;
+    s.beta1 = hp.beta1;
+    s.one_minus_beta1 = (float)(1.0 - b1);
+    s.beta2 = hp.beta2;
+    s.one_minus_beta2 = (float)(1.0 - b2);
+    s.decay = (float)(1.0 - (double)hp.lr * (double)hp.weight_decay);
+    s.step_size = (float)((double)hp.lr / bc1);
+    s.bc2_sqrt = (float)std::sqrt(bc2);
+    s.eps = hp.eps;
+    return s;
+}
+
+slide_status check_hparams(const slide_adam_hparams *hp)
+{
+    if (!hp)
+        return fail(SLIDE_ERR_INVALID_ARG, "hparams is NULL");
+    const float vals[6] = {hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay, hp->max_grad_norm};
+    for (float x : vals)
+        if (!std::isfinite(x))
+            return fail(SLIDE_ERR_INVALID_ARG, "hparams: non-finite value");
+    if (hp->lr < 0.0f)
+        return fail(SLIDE_ERR_INVALID_ARG, "hparams: lr < 0");
+    if (hp->beta1 < 0.0f || hp->beta1 >= 1.0f || hp->beta2 < 0.0f || hp->beta2 >= 1.0f)
+        return fail(SLIDE_ERR_INVALID_ARG, "hparams: betas must lie in [0, 1)");
+    if (hp->eps < 0.0f || hp->weight_decay < 0.0f)
+        return fail(SLIDE_ERR_INVALID_ARG, "hparams: eps and weight_decay must be >= 0");
+    return SLIDE_OK;
+}
+
+static bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+static slide_status check_config(const slide_config *cfg, int64_t *max_numel)
+{
+    if (!cfg)
+        return fail(SLIDE_ERR_INVALID_ARG, "config is NULL");
+    if (cfg->n_layers < 1 || !cfg->layer_numel)
+        return fail(SLIDE_ERR_INVALID_ARG, "config: n_layers must be >= 1 with a layer_numel array");
+    if (cfg->n_replicas < 1 || cfg->n_replicas > SLIDE_MAX_REPLICAS)
+        return fail(SLIDE_ERR_INVALID_ARG, "config: n_replicas must be in [1, 8]");
+    if (cfg->residency != SLIDE_RESIDENCY_HBM && cfg->residency != SLIDE_RESIDENCY_HOST_STREAMED)
+        return fail(SLIDE_ERR_INVALID_ARG, "config: unknown residency");
+    if (cfg->window_layers != 0 && cfg->window_layers != 2)
+        return fail(SLIDE_ERR_INVALID_ARG, "config: window_layers must be 2 (or 0 for the default 2)");
+    if (cfg->chunk_bytes < 0 || (cfg->chunk_bytes % 256) != 0)
+        return fail(SLIDE_ERR_INVALID_ARG, "config: chunk_bytes must be a non-negative multiple of 256");
+    if (cfg->flags & ~(uint32_t)SLIDE_FLAG_CHECK_FINITE)
+        return fail(SLIDE_ERR_INVALID_ARG, "config: unknown flag bits");
+    if (cfg->device < 0)
+        return fail(SLIDE_ERR_INVALID_ARG, "config: device < 0");
+    int64_t mx = 0;
+    for (int32_t l = 0; l < cfg->n_layers; ++l) {
+        const int64_t n = cfg->layer_numel[l];
+        if (n < 0 || n > ((int64_t)1 << 40))
+            return fail(SLIDE_ERR_INVALID_ARG, "config: layer_numel out of range [0, 2^40]");
+        if (n > mx)
+            mx = n;
+    }
+    *max_numel = mx;
+    return SLIDE_OK;
+}
+
+static size_t layer_state_bytes(int64_t n)
+{
+    return 3 * align_up((size_t)n * 4) + align_up((size_t)n * 2);
+}
+
+}  // namespace slide
+
+using namespace slide;
+
+extern "C" {
+
+int32_t slide_abi_version(void) { return SLIDE_ABI_VERSION; }
+
+const char *slide_last_error(void) { return g_last_error.c_str(); }
+
+slide_status slide_state_bytes(const slide_config *cfg, int64_t *device_bytes, int64_t *host_pinned_bytes)
+{
+    int64_t mx = 0;
+    slide_status rc = check_config(cfg, &mx);
+    if (rc != SLIDE_OK)
+        return rc;
+    size_t state = 0;
+    for (int32_t l = 0; l < cfg->n_layers; ++l)
+        state += layer_state_bytes(cfg->layer_numel[l]);
+    size_t dev = 0, host = 0;
+    if (cfg->residency == SLIDE_RESIDENCY_HBM) {
+        dev = state + (size_t)cfg->n_layers * scratch_bytes();
+    } else {
+        host = state;
+        dev = engine_device_bytes(*cfg, mx);
+    }
+    if (device_bytes)
+        *device_bytes = (int64_t)dev;
+    if (host_pinned_bytes)
+        *host_pinned_bytes = (int64_t)host;
+    clear_error();
+    return SLIDE_OK;
+}
+
+slide_status slide_state_create(const slide_config *cfg, slide_state **out)
+{
+    if (!out)
+        return fail(SLIDE_ERR_INVALID_ARG, "out is NULL");
+    int64_t mx = 0;
+    slide_status rc = check_config(cfg, &mx);
+    if (rc != SLIDE_OK)
+        return rc;
+    int ndev = 0;
+    cudaError_t e = cudaGetDeviceCount(&ndev);
+    if (e != cudaSuccess)
+        return fail_cuda(e, "cudaGetDeviceCount");
+    if (cfg->device >= ndev)
+        return fail(SLIDE_ERR_INVALID_ARG, "config: device ordinal out of range");
+    DeviceGuard guard(cfg->device);
+    if (!guard.ok)
+        return fail(SLIDE_ERR_CUDA, "cudaSetDevice failed");
+
+    slide_state *st = new (std::nothrow) slide_state();
+    if (!st)
+        return fail(SLIDE_ERR_OOM_HOST, "out of host memory for the state object");
+    st->cfg = *cfg;
+    st->cfg.layer_numel = nullptr;
+    if (st->cfg.window_layers == 0)
+        st->cfg.window_layers = 2;
+    if (st->cfg.timeout_ms == 0)
+        st->cfg.timeout_ms = 600000;
+    if (st->cfg.chunk_bytes == 0)
+        st->cfg.chunk_bytes = (int64_t)64 << 20;
+    st->device = cfg->device;
+    st->numel.assign(cfg->layer_numel, cfg->layer_numel + cfg->n_layers);
+    st->layers.resize(cfg->n_layers);
+
+    size_t state_bytes = 0;
+    for (int32_t l = 0; l < cfg->n_layers; ++l)
+        state_bytes += layer_state_bytes(st->numel[l]);
+
+    char *base = nullptr;
+    if (cfg->residency == SLIDE_RESIDENCY_HBM) {
+        st->dev_bytes = state_bytes + (size_t)cfg->n_layers * scratch_bytes();
+        e = cudaMalloc(&st->dev_arena, st->dev_bytes);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            delete st;
+            return fail(SLIDE_ERR_OOM_DEVICE, std::string("cudaMalloc of the HBM state (") +
+                                                  std::to_string(state_bytes) + " bytes) failed");
+        }
+        e = cudaMemset(st->dev_arena, 0, st->dev_bytes);
+        if (e != cudaSuccess) {
+            cudaFree(st->dev_arena);
+            delete st;
+            return fail_cuda(e, "cudaMemset of the HBM state");
+        }
+        base = (char *)st->dev_arena;
+    } else {
+        st->host_bytes = state_bytes;
+        e = cudaHostAlloc(&st->host_arena, st->host_bytes > 0 ? st->host_bytes : 1, cudaHostAllocDefault);
+        if (e != cudaSuccess || getenv("SLIDE_FAULT_PINNED_ALLOC")) {
+            // SLIDE_FAULT_PINNED_ALLOC injects this failure for tests of the
+            // clean-up path (nothing stays allocated).
+            if (e == cudaSuccess)
+                cudaFreeHost(st->host_arena);
+            cudaGetLastError();
+            delete st;
+            return fail(SLIDE_ERR_OOM_HOST, std::string("cudaHostAlloc of the pinned state (") +
+                                                std::to_string(state_bytes) + " bytes) failed");
+        }
+        memset(st->host_arena, 0, st->host_bytes);
+        base = (char *)st->host_arena;
+    }
+
+    size_t off = 0;
+    for (int32_t l = 0; l < cfg->n_layers; ++l) {
+        LayerState &L = st->layers[l];
+        const size_t n = (size_t)st->numel[l];
+        L.n = (int64_t)n;
+        L.theta = (float *)(base + off);
+        off += align_up(n * 4);
+        L.m = (float *)(base + off);
+        off += align_up(n * 4);
+        L.v = (float *)(base + off);
+        off += align_up(n * 4);
+        L.w = (uint16_t *)(base + off);
+        off += align_up(n * 2);
+    }
+    if (cfg->residency == SLIDE_RESIDENCY_HBM) {
+        for (int32_t l = 0; l < cfg->n_layers; ++l) {
+            LayerState &L = st->layers[l];
+            L.scratch.partials = (double *)(base + off);
+            L.scratch.coef = (float *)(base + off + align_up(sizeof(double) * kMaxPartials));
+            L.scratch.status = (unsigned *)(L.scratch.coef + 1);
+            off += scratch_bytes();
+        }
+    } else {
+        rc = engine_create(st);
+        if (rc != SLIDE_OK) {
+            cudaFreeHost(st->host_arena);
+            delete st;
+            return rc;
+        }
+    }
+    *out = st;
+    clear_error();
+    return SLIDE_OK;
+}
+
+void slide_state_destroy(slide_state *st)
+{
+    if (!st)
+        return;
+    DeviceGuard guard(st->device);
+    if (st->engine)
+        engine_destroy(st);
+    if (st->dev_arena) {
+        cudaDeviceSynchronize();
+        cudaFree(st->dev_arena);
+    }
+    if (st->host_arena)
+        cudaFreeHost(st->host_arena);
+    delete st;
+}
+
+static slide_status check_layer(slide_state *st, int32_t layer)
+{
+    if (!st)
+        return fail(SLIDE_ERR_INVALID_ARG, "state is NULL");
+    if (layer < 0 || layer >= (int32_t)st->layers.size())
+        return fail(SLIDE_ERR_INVALID_ARG, "layer index out of range");
+    return SLIDE_OK;
+}
+
+slide_status slide_layer_step(slide_state *st, int32_t layer, const void *const *grad_replicas,
+                              const slide_adam_hparams *hp, slide_stream_t stream, void *bf16_out)
+{
+    slide_status rc = check_layer(st, layer);
+    if (rc != SLIDE_OK)
+        return rc;
+    if (st->cfg.residency != SLIDE_RESIDENCY_HBM)
+        return fail(SLIDE_ERR_STATE, "slide_layer_step needs the HBM residency; use slide_model_step_streamed");
+    if ((rc = check_hparams(hp)) != SLIDE_OK)
+        return rc;
+    LayerState &L = st->layers[layer];
+    const int R = st->cfg.n_replicas;
+    if (!grad_replicas)
+        return fail(SLIDE_ERR_INVALID_ARG, "grad_replicas is NULL");
+    ReplicaPtrs g{};
+    for (int r = 0; r < R; ++r) {
+        g.p[r] = grad_replicas[r];
+        if (L.n > 0 && (!g.p[r] || !aligned16(g.p[r])))
+            return fail(SLIDE_ERR_INVALID_ARG, "gradient replica pointer is NULL or not 16-byte aligned");
+    }
+    uint16_t *w = bf16_out ? (uint16_t *)bf16_out : L.w;
+    if (!aligned16(w))
+        return fail(SLIDE_ERR_INVALID_ARG, "bf16_out is not 16-byte aligned");
+
+    const int64_t t = L.t + 1;
+    if (L.n > 0) {
+        DeviceGuard guard(st->device);
+        if (!guard.ok)
+            return fail(SLIDE_ERR_CUDA, "cudaSetDevice failed");
+        cudaStream_t s = (cudaStream_t)stream;
+        const AdamScalars sc = adam_scalars_for(*hp, t);
+        const bool clip = hp->max_grad_norm > 0.0f;
+        const bool check = (st->cfg.flags & SLIDE_FLAG_CHECK_FINITE) != 0;
+        int n_partials = 0;
+        cudaError_t e;
+        if (st->trace[0])
+            cudaEventRecord(st->trace[0], s);
+        if (clip) {
+            e = launch_grad_sqnorm(g, R, L.n, L.scratch, &n_partials, st->device, s);
+            if (e != cudaSuccess)
+                return fail_cuda(e, "grad_sqnorm launch");
+        }
+        if (st->trace[1])
+            cudaEventRecord(st->trace[1], s);
+        e = launch_grad_reduce_adamw_cast(g, R, L.n, L.theta, L.m, L.v, w, sc,
+                                          (clip || check) ? &L.scratch : nullptr, n_partials,
+                                          clip ? hp->max_grad_norm : 0.0f, check, st->device, s);
+        if (e != cudaSuccess)
+            return fail_cuda(e, "grad_reduce_adamw_cast launch");
+        if (st->trace[2])
+            cudaEventRecord(st->trace[2], s);
+    }
+    L.t = t;
+    clear_error();
+    return SLIDE_OK;
+}
+
+static void refresh_aborted(slide_state *st)
+{
+    if (!st->aborted)
+        return;
+    for (const LayerState &L : st->layers)
+        if (L.t != st->layers[0].t)
+            return;
+    st->aborted = false;
+}
+
+slide_status slide_layer_set(slide_state *st, int32_t layer, const float *master, const float *m,
+                             const float *v, int64_t step)
+{
+    slide_status rc = check_layer(st, layer);
+    if (rc != SLIDE_OK)
+        return rc;
+    if (step < 0)
+        return fail(SLIDE_ERR_INVALID_ARG, "step must be >= 0");
+    LayerState &L = st->layers[layer];
+    DeviceGuard guard(st->device);
+    if (!guard.ok)
+        return fail(SLIDE_ERR_CUDA, "cudaSetDevice failed");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess)
+        return fail_cuda(e, "cudaDeviceSynchronize");
+    const size_t bytes = (size_t)L.n * 4;
+    const float *src[3] = {master, m, v};
+    float *dst[3] = {L.theta, L.m, L.v};
+    for (int k = 0; k < 3; ++k) {
+        if (!src[k] || bytes == 0)
+            continue;
+        e = cudaMemcpy(dst[k], src[k], bytes, cudaMemcpyDefault);
+        if (e != cudaSuccess)
+            return fail_cuda(e, "cudaMemcpy in slide_layer_set");
+    }
+    if (master && L.n > 0) {
+        // The pinned host arrays of the streamed residency are device-accessible too.
+        e = launch_cast_bf16(L.theta, L.w, L.n, 0);
+        if (e == cudaSuccess)
+            e = cudaDeviceSynchronize();
+        if (e != cudaSuccess)
+            return fail_cuda(e, "bf16 cast in slide_layer_set");
+    }
+    L.t = step;
+    refresh_aborted(st);
+    clear_error();
+    return SLIDE_OK;
+}
+
+slide_status slide_layer_get(slide_state *st, int32_t layer, float *master, float *m, float *v,
+                             uint16_t *bf16, int64_t *step)
+{
+    slide_status rc = check_layer(st, layer);
+    if (rc != SLIDE_OK)
+        return rc;
+    LayerState &L = st->layers[layer];
+    DeviceGuard guard(st->device);
+    if (!guard.ok)
+        return fail(SLIDE_ERR_CUDA, "cudaSetDevice failed");
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess)
+        return fail_cuda(e, "cudaDeviceSynchronize");
+    const void *src[4] = {L.theta, L.m, L.v, L.w};
+    void *dst[4] = {master, m, v, bf16};
+    const size_t bytes[4] = {(size_t)L.n * 4, (size_t)L.n * 4, (size_t)L.n * 4, (size_t)L.n * 2};
+    for (int k = 0; k < 4; ++k) {
+        if (!dst[k] || bytes[k] == 0)
+            continue;
+        e = cudaMemcpy(dst[k], src[k], bytes[k], cudaMemcpyDefault);
+        if (e != cudaSuccess)
+            return fail_cuda(e, "cudaMemcpy in slide_layer_get");
+    }
+    if (step)
+        *step = L.t;
+    clear_error();
+    return SLIDE_OK;
+}
+
+slide_status slide_layer_ptrs(slide_state *st, int32_t layer, float **master, float **m, float **v,
+                              uint16_t **bf16)
+{
+    slide_status rc = check_layer(st, layer);
+    if (rc != SLIDE_OK)
+        return rc;
+    LayerState &L = st->layers[layer];
+    if (master)
+        *master = L.theta;
+    if (m)
+        *m = L.m;
+    if (v)
+        *v = L.v;
+    if (bf16)
+        *bf16 = L.w;
+    clear_error();
+    return SLIDE_OK;
+}
+
+slide_status slide_layer_last_clip_coef(slide_state *st, int32_t layer, float *coef)
+{
+    slide_status rc = check_layer(st, layer);
+    if (rc != SLIDE_OK)
+        return rc;
+    if (!coef)
+        return fail(SLIDE_ERR_INVALID_ARG, "coef is NULL");
+    LayerState &L = st->layers[layer];
+    if (!L.scratch.coef)
+        return fail(SLIDE_ERR_STATE, "no clip scratch for this residency");
+    DeviceGuard guard(st->device);
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess)
+        e = cudaMemcpy(coef, L.scratch.coef, sizeof(float), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess)
+        return fail_cuda(e, "reading the clip coefficient");
+    if (*coef == 0.0f)  // never written: the arena starts zeroed
+        *coef = 1.0f;
+    clear_error();
+    return SLIDE_OK;
+}
+
+slide_status slide_layer_status(slide_state *st, int32_t layer)
+{
+    slide_status rc = check_layer(st, layer);
+    if (rc != SLIDE_OK)
+        return rc;
+    LayerState &L = st->layers[layer];
+    if (!(st->cfg.flags & SLIDE_FLAG_CHECK_FINITE) || !L.scratch.status)
+        return SLIDE_OK;
+    DeviceGuard guard(st->device);
+    unsigned word = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess)
+        e = cudaMemcpy(&word, L.scratch.status, sizeof word, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && word)
+        e = cudaMemset(L.scratch.status, 0, sizeof word);
+    if (e != cudaSuccess)
+        return fail_cuda(e, "reading the status word");
+    if (word & 1u)
+        return fail(SLIDE_ERR_NONFINITE, "a non-finite mean gradient was seen");
+    clear_error();
+    return SLIDE_OK;
+}
+
+slide_status slide_trace_events(slide_state *st, void *ev_prepass_start, void *ev_update_start,
+                                void *ev_update_stop)
+{
+    if (!st)
+        return fail(SLIDE_ERR_INVALID_ARG, "state is NULL");
+    st->trace[0] = (cudaEvent_t)ev_prepass_start;
+    st->trace[1] = (cudaEvent_t)ev_update_start;
+    st->trace[2] = (cudaEvent_t)ev_update_stop;
+    clear_error();
+    return SLIDE_OK;
+}
+
+slide_status slide_model_step_streamed(slide_state *st, slide_grad_fn fn, void *user,
+                                       const slide_adam_hparams *hp)
+{
+    if (!st)
+        return fail(SLIDE_ERR_INVALID_ARG, "state is NULL");
+    if (st->cfg.residency != SLIDE_RESIDENCY_HOST_STREAMED || !st->engine)
+        return fail(SLIDE_ERR_STATE, "slide_model_step_streamed needs the host-streamed residency");
+    if (!fn)
+        return fail(SLIDE_ERR_INVALID_ARG, "grad_fn is NULL");
+    slide_status rc = check_hparams(hp);
+    if (rc != SLIDE_OK)
+        return rc;
+    if (st->aborted)
+        return fail(SLIDE_ERR_ABORTED, "an earlier sweep was aborted; restore a common version with slide_layer_set");
+    for (const LayerState &L : st->layers)
+        if (L.t != st->layers[0].t)
+            return fail(SLIDE_ERR_VERSION, "units carry different step counts (same-version invariant)");
+    DeviceGuard guard(st->device);
+    if (!guard.ok)
+        return fail(SLIDE_ERR_CUDA, "cudaSetDevice failed");
+    rc = engine_step(st, fn, user, *hp);
+    if (rc == SLIDE_OK)
+        clear_error();
+    return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,51 @@
+// slide_kernels.h — internal interface between the C ABI (slide_api.cu), the
+// streaming engine (stream_engine.cu) and the kernels
+// (grad_reduce_adamw_cast.cu).  Not installed; not part of the ABI.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace slide {
+
+constexpr int kMaxReplicas = 8;
+constexpr int kMaxPartials = 4096;  // per-block partial sums of the clip pre-pass
+
+// Per-step FP32 scalars of the AdamW update (formed in double on the host,
+// rounded once; see adam_scalars_for in slide_api.cu).
+struct AdamScalars {
+    float beta1, one_minus_beta1, beta2, one_minus_beta2;
+    float decay;      // 1 - lr*wd
+    float step_size;  // lr / (1 - beta1^t)
+    float bc2_sqrt;   // sqrt(1 - beta2^t)
+    float eps;
+};
+
+struct ReplicaPtrs {
+    const void *p[kMaxReplicas];
+};
+
+// Device scratch of one layer's clip reduction.
+struct ClipScratch {
+    double *partials;  // [kMaxPartials]
+    float *coef;       // last coefficient used (written by block 0)
+    unsigned *status;  // bit 0: a non-finite mean gradient was seen
+};
+
+// Clip pre-pass: per-block partial sums of the squared replica mean into
+// scratch.partials; returns the number of partials written via *n_partials.
+cudaError_t launch_grad_sqnorm(const ReplicaPtrs &g, int R, int64_t n, const ClipScratch &scratch,
+                               int *n_partials, int device, cudaStream_t stream);
+
+// Fused step.  When max_norm > 0 the kernel reduces the n_partials partial
+// sums (in a fixed order, identically in every block) to the clip coefficient.
+// status may be NULL; when check_finite is set and status is not NULL a
+// non-finite mean gradient sets bit 0 of *status.
+cudaError_t launch_grad_reduce_adamw_cast(const ReplicaPtrs &g, int R, int64_t n, float *theta,
+                                          float *m, float *v, uint16_t *w, const AdamScalars &s,
+                                          const ClipScratch *clip, int n_partials, float max_norm,
+                                          bool check_finite, int device, cudaStream_t stream);
+
+// w[i] = bf16_rne(src[i]) (used when a caller overwrites a master copy).
+cudaError_t launch_cast_bf16(const float *src, uint16_t *w, int64_t n, cudaStream_t stream);
+
+}  // namespace slide

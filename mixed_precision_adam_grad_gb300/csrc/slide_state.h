@@ -1,0 +1,81 @@
+// slide_state.h — internal definition of the opaque slide_state and helpers
+// shared by slide_api.cu and stream_engine.cu.  Not part of the ABI.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "slide.h"
+#include "slide_kernels.h"
+
+namespace slide {
+
+struct StreamEngine;  // stream_engine.cu
+
+struct LayerState {
+    int64_t n = 0;
+    float *theta = nullptr;  // HBM or pinned host (streamed)
+    float *m = nullptr;
+    float *v = nullptr;
+    uint16_t *w = nullptr;
+    ClipScratch scratch{};   // device scratch of the clip pre-pass (HBM residency)
+    int64_t t = 0;           // updates applied so far
+};
+
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess)
+            prev = -1;
+        ok = cudaSetDevice(dev) == cudaSuccess;
+    }
+    ~DeviceGuard()
+    {
+        if (prev >= 0)
+            cudaSetDevice(prev);
+    }
+};
+
+}  // namespace slide
+
+struct slide_state {
+    slide_config cfg{};
+    std::vector<int64_t> numel;
+    std::vector<slide::LayerState> layers;
+    int device = 0;
+    void *dev_arena = nullptr;   // one cudaMalloc for all device arrays
+    size_t dev_bytes = 0;
+    void *host_arena = nullptr;  // one cudaHostAlloc (streamed residency)
+    size_t host_bytes = 0;
+    slide::StreamEngine *engine = nullptr;
+    bool aborted = false;
+    cudaEvent_t trace[3] = {nullptr, nullptr, nullptr};  // prepass start, update start, update stop
+};
+
+namespace slide {
+
+// Thread-local last-error message and status helpers (slide_api.cu).
+slide_status fail(slide_status code, const std::string &msg);
+slide_status fail_cuda(cudaError_t e, const char *what);
+void clear_error();
+
+// Per-step scalars for update t (1-based) from the FP32 hyper-parameters.
+AdamScalars adam_scalars_for(const slide_adam_hparams &hp, int64_t t);
+slide_status check_hparams(const slide_adam_hparams *hp);
+
+// Byte layout shared by slide_state_bytes and slide_state_create.
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+inline size_t scratch_bytes() { return align_up(sizeof(double) * kMaxPartials) + kAlign; }
+
+// Streamed residency (stream_engine.cu).
+slide_status engine_create(slide_state *st);
+void engine_destroy(slide_state *st);
+size_t engine_device_bytes(const slide_config &cfg, int64_t max_numel);
+slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const slide_adam_hparams &hp);
+
+}  // namespace slide

@@ -1,0 +1,119 @@
+"""Helpers shared by the GPU parity tests, the smoke check and the benchmark's
+oracle legs: drive the CUDA path through the C ABI on seeded synthetic inputs,
+drive the oracle on the same inputs (generated on the host, bit-identical),
+and compare with the tolerance the workloads fix:
+
+  FP32 master, m, v:  max |gpu - oracle| <= 2e-6 * (1 + |oracle|)
+  BF16 compute copy:  at most 1 BF16 ulp apart (bit patterns differ by <= 1)
+
+and, sharper than that gate, report how many FP32 values are not bit-equal.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+import synth
+
+TOL_REL = 2e-6
+
+
+def hp_oracle(w):
+    return oracle.hparams(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_grad_norm)
+
+
+def compare_fp32(name, got, want, tol=TOL_REL):
+    got = np.asarray(got, np.float32)
+    want = np.asarray(want, np.float32)
+    diff = np.abs(got.astype(np.float64) - want.astype(np.float64))
+    bound = tol * (1.0 + np.abs(want.astype(np.float64)))
+    bad = ~(diff <= bound)
+    info = {
+        "name": name,
+        "n": int(got.size),
+        "max_abs": float(diff.max()) if diff.size else 0.0,
+        "not_bit_equal": int(np.count_nonzero(got.view(np.uint32) != want.view(np.uint32))),
+        "violations": int(np.count_nonzero(bad)),
+    }
+    return info
+
+
+def compare_bf16(name, got, want):
+    a = np.asarray(got, np.uint16).astype(np.int32)
+    b = np.asarray(want, np.uint16).astype(np.int32)
+    # distance in units in the last place on the BF16 lattice (same sign)
+    ia = np.where(a & 0x8000, -(a & 0x7FFF), a)
+    ib = np.where(b & 0x8000, -(b & 0x7FFF), b)
+    d = np.abs(ia - ib)
+    return {"name": name, "n": int(a.size), "max_ulp": int(d.max()) if d.size else 0,
+            "not_bit_equal": int(np.count_nonzero(a != b)), "violations": int(np.count_nonzero(d > 1))}
+
+
+def assert_parity(reports):
+    for r in reports:
+        assert r["violations"] == 0, r
+
+
+def unit_grad_host(w, unit_index, step, replica, idx=None):
+    """BF16 gradient replica of a unit at `step` on the host (whole unit or the
+    given sorted element indices)."""
+    u = w.units[unit_index]
+    sp = synth.spec(w.seed, w.grad_kind, w.zero_prob)
+    scales = w.tensor_scales(unit_index)
+    if idx is None:
+        out = np.empty(u.numel, np.uint16)
+        for (off, n), sc in zip(u.segments(), scales):
+            out[off:off + n] = synth.grad(n, sp, unit_index, step, replica, sc, offset=off)
+        return out
+    idx = np.asarray(idx, np.int64)
+    out = np.empty(idx.size, np.uint16)
+    bounds = np.cumsum([0] + [n for _, n in u.tensors])
+    for k, sc in enumerate(scales):
+        sel = (idx >= bounds[k]) & (idx < bounds[k + 1])
+        if sel.any():
+            out[sel] = synth.gather_grad(idx[sel], sp, unit_index, step, replica, sc)
+    return out
+
+
+def unit_grad_dev(w, unit_index, step, replica, ptr, stream=0):
+    u = w.units[unit_index]
+    sp = synth.spec(w.seed, w.grad_kind, w.zero_prob)
+    for (off, n), sc in zip(u.segments(), w.tensor_scales(unit_index)):
+        synth.dev_grad(ptr + 2 * off, n, sp, unit_index, step, replica, sc, offset=off, stream=stream)
+
+
+def sample_indices(n, k, seed=1234, extra=()):
+    """Sorted unique sample: k random indices, the first and last 4096, extras."""
+    rng = np.random.default_rng(seed)
+    parts = [rng.integers(0, n, size=min(k, n)), np.arange(min(4096, n)),
+             np.arange(max(0, n - 4096), n)]
+    if len(extra):
+        e = np.asarray(extra, np.int64)
+        parts.append(e[(e >= 0) & (e < n)])
+    return np.unique(np.concatenate(parts).astype(np.int64))
+
+
+def oracle_full_coefs(w, unit_index, steps):
+    """Clip coefficient of each step (by the oracle over the whole unit)."""
+    hp = hp_oracle(w)
+    coefs = {}
+    for t in steps:
+        reps = [unit_grad_host(w, unit_index, t, r) for r in range(w.R)]
+        gm = oracle.grad_mean(reps)
+        coefs[t] = oracle.clip_coef(oracle.grad_sqnorm(gm), hp.max_grad_norm)
+        del reps, gm
+    return coefs
+
+
+def oracle_sampled(w, unit_index, idx, first_step, last_step, theta, m, v, coefs=None):
+    """Run the oracle on the sampled elements (in place) for steps
+    first_step..last_step.  With the clip on, coefs[t] must hold the oracle's
+    whole-unit coefficient of step t.  Returns the BF16 copy."""
+    hp = hp_oracle(w)
+    wbf = np.zeros(idx.size, np.uint16)
+    for t in range(first_step, last_step + 1):
+        reps = [unit_grad_host(w, unit_index, t, r, idx) for r in range(w.R)]
+        gm = oracle.grad_mean(reps)
+        coef = coefs[t] if (w.max_grad_norm > 0) else 1.0
+        oracle.adamw_update(gm, coef, theta, m, v, wbf, hp, t)
+    return wbf

@@ -1,0 +1,304 @@
+"""GPU parity: the CUDA path (through the C ABI) against the oracle, element by
+element on identical seeded inputs.
+
+Small sizes compare every element (they span several blocks' tiles and a
+ragged tail); the full-size workloads compare sampled elements, which the
+oracle computes one by one (the update is elementwise once the clip
+coefficient, which the oracle forms over the whole layer, is known).
+
+Gate: |gpu - oracle| <= 2e-6*(1+|oracle|) on FP32 master, m, v after every
+step, and <= 1 BF16 ulp on the emitted copy.  Without the clip the two
+follow the same FP32 operation sequence, so those cases also require bit
+equality.
+"""
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import oracle  # noqa: E402
+import synth  # noqa: E402
+from synth import workloads as W  # noqa: E402
+import parity_util as pu  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def S():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import mixed_precision_adam_grad_gb300 as S
+    return S
+
+
+def dev_u16(n):
+    return torch.empty(max(n, 1) + 64, dtype=torch.int16, device="cuda")
+
+
+def to_np_u16(t, n):
+    return t[:n].cpu().numpy().view(np.uint16)
+
+
+# -------------------------------------------------------------- generator ----
+
+def test_generator_device_matches_host(S):
+    n, off = (1 << 20) + 3, 12345
+    out = torch.empty(n, dtype=torch.float32, device="cuda")
+    synth.dev_master(out.data_ptr(), n, seed=9, unit=3, scale=0.02, offset=off)
+    torch.cuda.synchronize()
+    host = synth.master(n, seed=9, unit=3, scale=0.02, offset=off)
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), host.view(np.uint32))
+    for kind, zp in ((synth.GRAD_NORMAL, 0.0), (synth.GRAD_STUDENT3, 0.001)):
+        sp = synth.spec(5, kind, zp)
+        g = dev_u16(n)
+        synth.dev_grad(g.data_ptr(), n, sp, 2, 7, 3, 1e-3, offset=off)
+        torch.cuda.synchronize()
+        assert np.array_equal(to_np_u16(g, n), synth.grad(n, sp, 2, 7, 3, 1e-3, offset=off))
+
+
+# ------------------------------------------------------ small, every element ----
+
+def run_small(S, sizes, R, clip, steps=4, seed=11, flags=0, bf16_external=False):
+    """Multi-layer state with the given layer sizes; `steps` steps of every
+    layer on fresh seeded grads; full comparison with the oracle after each."""
+    w = W.Workload("small", [W.Unit(f"l{i}", [("flat", n)]) for i, n in enumerate(sizes)],
+                   R=R, steps=steps, seed=seed, max_grad_norm=clip, lr=1e-3)
+    hp_dev = S.hparams(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_grad_norm)
+    hp_or = pu.hp_oracle(w)
+    st = S.slide_state_create(sizes, R, flags=flags)
+    reports = []
+    try:
+        ref = []
+        for li, n in enumerate(sizes):
+            th0 = synth.master(n, seed, unit=li)
+            S.slide_layer_set(st, li, master=th0, step=0)
+            ref.append([th0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32),
+                        np.zeros(n, np.uint16)])
+        grads = [dev_u16(max(sizes)) for _ in range(R)]
+        outs = [dev_u16(n) for n in sizes] if bf16_external else None
+        for t in range(1, steps + 1):
+            for li, n in enumerate(sizes):
+                for r in range(R):
+                    pu.unit_grad_dev(w, li, t, r, grads[r].data_ptr())
+                S.slide_layer_step(st, li, grads, hp_dev, None, outs[li] if outs else None)
+                host_g = [pu.unit_grad_host(w, li, t, r) for r in range(R)]
+                coef = oracle.layer_step(host_g, *ref[li][:3], ref[li][3], hp_or, t)
+                th, m, v = (np.empty(n, np.float32) for _ in range(3))
+                wb = np.empty(n, np.uint16)
+                tt = S.slide_layer_get(st, li, th, m, v, wb)
+                assert tt == t
+                if bf16_external:
+                    torch.cuda.synchronize()
+                    wb = to_np_u16(outs[li], n)
+                rep = [pu.compare_fp32(f"theta l{li} t{t}", th, ref[li][0]),
+                       pu.compare_fp32(f"m l{li} t{t}", m, ref[li][1]),
+                       pu.compare_fp32(f"v l{li} t{t}", v, ref[li][2]),
+                       pu.compare_bf16(f"w l{li} t{t}", wb, ref[li][3])]
+                pu.assert_parity(rep)
+                # the emitted copy is the RNE rounding of the GPU's own master
+                assert np.array_equal(wb, oracle.f32_to_bf16(th))
+                if clip > 0 and n > 0:
+                    gc = S.slide_layer_last_clip_coef(st, li)
+                    assert abs(gc - coef) <= 2 * np.spacing(np.float32(coef)), (gc, coef)
+                reports += rep
+    finally:
+        S.slide_state_destroy(st)
+    return reports
+
+
+SIZES = [1, 7, 8, 9, 1000, 1001, 4096 + 3, (1 << 20) + 5]
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 5, 8])
+def test_small_parity_no_clip_bit_exact(S, R):
+    reps = run_small(S, SIZES, R, clip=0.0)
+    for r in reps:
+        assert r["not_bit_equal"] == 0, r
+
+
+@pytest.mark.parametrize("R", [1, 4, 8])
+@pytest.mark.parametrize("clip", [1e-3, 1e3])
+def test_small_parity_clip(S, R, clip):
+    reps = run_small(S, [9, 4096 + 3, (1 << 20) + 5, 3 * (1 << 20) + 1], R, clip=clip)
+    if clip > 1.0:  # norm far below the threshold: coefficient exactly 1
+        for r in reps:
+            assert r["not_bit_equal"] == 0, r
+
+
+def test_external_bf16_out_and_empty_layer(S):
+    run_small(S, [0, 5, 4099], 2, clip=0.5, bf16_external=True)
+
+
+def test_prewarm_handoff_from_oracle(S):
+    """m and v from 5 oracle steps handed to the state (t = 5), then GPU steps
+    6..9 compared with oracle steps 6..9."""
+    n, R = 70001, 4
+    w = W.Workload("prewarm", [W.Unit("l", [("flat", n)])], R=R, steps=4, seed=21, max_grad_norm=1.0,
+                   prewarm_steps=5)
+    hp_or = pu.hp_oracle(w)
+    th = synth.master(n, w.seed)
+    m, v = np.zeros(n, np.float32), np.zeros(n, np.float32)
+    for t in range(1, 6):
+        oracle.layer_step([pu.unit_grad_host(w, 0, t, r) for r in range(R)], th, m, v, None, hp_or, t)
+    st = S.slide_state_create([n], R)
+    try:
+        S.slide_layer_set(st, 0, th, m, v, step=5)
+        grads = [dev_u16(n) for _ in range(R)]
+        hp = S.hparams(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_grad_norm)
+        wb = np.zeros(n, np.uint16)
+        for t in range(6, 10):
+            for r in range(R):
+                pu.unit_grad_dev(w, 0, t, r, grads[r].data_ptr())
+            S.slide_layer_step(st, 0, grads, hp)
+            oracle.layer_step([pu.unit_grad_host(w, 0, t, r) for r in range(R)], th, m, v, wb, hp_or, t)
+        gt, gm, gv = (np.empty(n, np.float32) for _ in range(3))
+        gw = np.empty(n, np.uint16)
+        assert S.slide_layer_get(st, 0, gt, gm, gv, gw) == 9
+        pu.assert_parity([pu.compare_fp32("theta", gt, th), pu.compare_fp32("m", gm, m),
+                          pu.compare_fp32("v", gv, v), pu.compare_bf16("w", gw, wb)])
+    finally:
+        S.slide_state_destroy(st)
+
+
+def test_write_set_is_exactly_the_layer(S):
+    """A step of layer 0 touches exactly its own n elements: the next layer's
+    arrays and an external output's bytes past n keep their sentinel values."""
+    n0, n1, R = 4103, 333, 3
+    st = S.slide_state_create([n0, n1], R)
+    try:
+        sent = np.full(n1, np.nan, np.float32)
+        S.slide_layer_set(st, 1, sent, sent, sent, step=0)
+        w = W.Workload("ws", [W.Unit("a", [("f", n0)])], R=R, steps=1, seed=3)
+        grads = [dev_u16(n0) for _ in range(R)]
+        for r in range(R):
+            pu.unit_grad_dev(w, 0, 1, r, grads[r].data_ptr())
+        out = torch.full((n0 + 64,), 0x7ABC, dtype=torch.int16, device="cuda")
+        S.slide_layer_step(st, 0, grads, S.hparams(), None, out)
+        torch.cuda.synchronize()
+        tail = out[n0:].cpu().numpy()
+        assert np.all(tail == 0x7ABC)
+        a, b, c = (np.empty(n1, np.float32) for _ in range(3))
+        S.slide_layer_get(st, 1, a, b, c)
+        assert np.isnan(a).all() and np.isnan(b).all() and np.isnan(c).all()
+    finally:
+        S.slide_state_destroy(st)
+
+
+def test_nonfinite_flag_reports_without_fault(S):
+    n, R = 1000, 2
+    st = S.slide_state_create([n], R, flags=S.SLIDE_FLAG_CHECK_FINITE)
+    try:
+        g = [torch.zeros(n + 8, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+        S.slide_layer_step(st, 0, g, S.hparams())
+        assert S.slide_layer_status(st, 0) == S.SLIDE_OK
+        g[1][17] = float("nan")
+        S.slide_layer_step(st, 0, g, S.hparams())
+        assert S.slide_layer_status(st, 0) == S.SLIDE_ERR_NONFINITE
+        assert S.slide_layer_status(st, 0) == S.SLIDE_OK  # the mark is cleared
+    finally:
+        S.slide_state_destroy(st)
+
+
+def test_argument_errors(S):
+    n, R = 100, 2
+    st = S.slide_state_create([n], R)
+    try:
+        g = [torch.zeros(n + 16, dtype=torch.bfloat16, device="cuda") for _ in range(R)]
+        with pytest.raises(S.SlideError) as e:
+            S.slide_layer_step(st, 0, [g[0], g[1].data_ptr() + 2], S.hparams())
+        assert e.value.status == S.SLIDE_ERR_INVALID_ARG
+        with pytest.raises(S.SlideError) as e:
+            S.slide_layer_step(st, 1, g, S.hparams())
+        assert e.value.status == S.SLIDE_ERR_INVALID_ARG
+        with pytest.raises(S.SlideError) as e:
+            S.slide_layer_step(st, 0, g, S.hparams(beta1=1.0))
+        assert e.value.status == S.SLIDE_ERR_INVALID_ARG
+        with pytest.raises(S.SlideError) as e:
+            S.slide_model_step_streamed(st, 1, None, S.hparams())
+        assert e.value.status == S.SLIDE_ERR_STATE
+        # nothing was enqueued and t did not move
+        assert S.slide_layer_get(st, 0) == 0
+    finally:
+        S.slide_state_destroy(st)
+
+
+def test_state_allocation_matches_accounting(S):
+    """cudaMemGetInfo sees the arena that slide_state_bytes predicts."""
+    sizes = [100_000_000, 1]
+    dev_bytes, host_bytes = S.slide_state_bytes(sizes, 4)
+    assert host_bytes == 0
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    st = S.slide_state_create(sizes, 4)
+    try:
+        free1, _ = torch.cuda.mem_get_info()
+        used = free0 - free1
+        assert dev_bytes <= used <= dev_bytes + (64 << 20), (used, dev_bytes)
+    finally:
+        S.slide_state_destroy(st)
+
+
+# -------------------------------------------- full-size workloads, sampled ----
+
+def run_full_size(S, w, n_samples=200_000):
+    """The workload's single HBM-resident unit at full size, in the launch
+    configuration the benchmark times (the library picks it); the oracle on
+    sampled elements, with whole-unit clip coefficients when the clip is on."""
+    assert len(w.units) == 1
+    n = w.units[0].numel
+    bounds = np.cumsum([0] + [k for _, k in w.units[0].tensors])
+    idx = pu.sample_indices(n, n_samples, extra=np.concatenate([bounds - 1, bounds]))
+    t0 = 0
+    th_s = synth.gather_master(idx, w.seed)
+    m_s, v_s = np.zeros(idx.size, np.float32), np.zeros(idx.size, np.float32)
+    st = S.slide_state_create([n], w.R)
+    try:
+        th_d = S.slide_layer_ptrs(st, 0)[0]
+        synth.dev_master(th_d, n, w.seed)
+        torch.cuda.synchronize()
+        coefs = None
+        if w.max_grad_norm > 0:
+            coefs = pu.oracle_full_coefs(w, 0, range(1, w.prewarm_steps + w.steps + 1))
+        if w.prewarm_steps:
+            # pre-warm by the oracle over the whole unit, handed to the state
+            hp_or = pu.hp_oracle(w)
+            th = synth.master(n, w.seed)
+            m, v = np.zeros(n, np.float32), np.zeros(n, np.float32)
+            for t in range(1, w.prewarm_steps + 1):
+                reps = [pu.unit_grad_host(w, 0, t, r) for r in range(w.R)]
+                gm = oracle.grad_mean(reps)
+                del reps
+                oracle.adamw_update(gm, coefs[t], th, m, v, None, hp_or, t)
+                del gm
+            S.slide_layer_set(st, 0, th, m, v, step=w.prewarm_steps)
+            th_s, m_s, v_s = th[idx].copy(), m[idx].copy(), v[idx].copy()
+            del th, m, v
+            t0 = w.prewarm_steps
+        grads = [dev_u16(n) for _ in range(w.R)]
+        hp = S.hparams(*w.hparams_tuple())
+        for t in range(t0 + 1, t0 + w.steps + 1):
+            for r in range(w.R):
+                pu.unit_grad_dev(w, 0, t, r, grads[r].data_ptr())
+            S.slide_layer_step(st, 0, grads, hp)
+            if coefs is not None:
+                gc = S.slide_layer_last_clip_coef(st, 0)
+                assert abs(gc - coefs[t]) <= 2 * np.spacing(np.float32(coefs[t])), (t, gc, coefs[t])
+        w_s = pu.oracle_sampled(w, 0, idx, t0 + 1, t0 + w.steps, th_s, m_s, v_s, coefs)
+        th_a, m_a, v_a = (np.empty(n, np.float32) for _ in range(3))
+        w_a = np.empty(n, np.uint16)
+        assert S.slide_layer_get(st, 0, th_a, m_a, v_a, w_a) == t0 + w.steps
+        th_g, m_g, v_g, w_g = th_a[idx], m_a[idx], v_a[idx], w_a[idx]
+        del th_a, m_a, v_a, w_a
+        rep = [pu.compare_fp32("theta", th_g, th_s), pu.compare_fp32("m", m_g, m_s),
+               pu.compare_fp32("v", v_g, v_s), pu.compare_bf16("w", w_g, w_s)]
+        pu.assert_parity(rep)
+        assert np.array_equal(w_g, oracle.f32_to_bf16(th_g))
+        return rep
+    finally:
+        S.slide_state_destroy(st)
+
+
+@pytest.mark.parametrize("cfg", [1, 2, 3])
+def test_full_size_workload_sampled(S, cfg):
+    rep = run_full_size(S, W.ALL[cfg]())
+    print(rep)
