@@ -32,7 +32,6 @@ if ROOT not in sys.path:
 
 METRIC = "LayerAdam Gparam/s & HBM GB/s vs ~8 TB/s; host-streamed s/step vs link BW"
 UNIT = "Gparam/s"
-N_BATCHES = 4
 
 
 def parse_args():
@@ -46,6 +45,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--batches", type=int, default=4,
+                    help="pre-generated gradient batches cycled by the steps (1 for small profiling runs)")
     ap.add_argument("--soak-s", type=float, default=1.5,
                     help="seconds of untimed steps before the timed region (clocks settle, samples)")
     args = ap.parse_args()
@@ -214,7 +215,7 @@ def run_ours(args):
         th_d = S.slide_layer_ptrs(st, 0)[0]
         synth.dev_master(th_d, n, w.seed + 100 * rank, stream=stream.cuda_stream)
         batches = []
-        for b in range(N_BATCHES):
+        for b in range(args.batches):
             reps = [torch.empty(n + 64, dtype=torch.int16, device="cuda") for _ in range(R)]
             for r, t in enumerate(reps):
                 for (off, ln), sc in zip(w.units[0].segments(), w.tensor_scales(0)):
@@ -225,7 +226,7 @@ def run_ours(args):
         torch.cuda.synchronize()
 
         def step(i):
-            S.slide_layer_step(st, 0, batches[i % N_BATCHES], hp, stream)
+            S.slide_layer_step(st, 0, batches[i % len(batches)], hp, stream)
 
         for i in range(args.warmup):
             step(i)
@@ -352,7 +353,7 @@ def run_ours(args):
         "config": {"workload": w.name, "description": w.description, "params": n, "replicas": R,
                    "max_grad_norm": w.max_grad_norm, "parallelism": f"replicas-only x{world}",
                    "l2": f"inputs larger than L2: each step touches {step_bytes / 1e9:.2f} GB; "
-                         f"{N_BATCHES} gradient batches cycled",
+                         f"{args.batches} gradient batches cycled",
                    "clock_samples": "nvidia-smi every 200 ms over a soak of the same step and the "
                                     "timed region"},
         "hbm_gbs": step_bytes / (ms_step * 1e-3) / 1e9,

@@ -114,9 +114,12 @@ typedef struct {
 typedef struct slide_state slide_state; /* opaque; owns all of its memory */
 
 /* Gradient callback of the streamed step (stands in for a layer's backward):
- * fill the R BF16 replica buffers of unit `layer` (device pointers, each
- * layer_numel[layer] elements, owned by the state) with work enqueued on
- * `stream`.  Return 0 on success; any other value aborts the sweep. */
+ * fill the R BF16 replica buffers replica_dev_ptrs[0..R-1] of unit `layer`
+ * (device pointers into the window, each layer_numel[layer] elements, owned by
+ * the state) with work enqueued on `stream`.  replica_dev_ptrs[R] points to
+ * the unit's FP32 master weights in the window, the version being updated
+ * (read-only), as a backward pass would read them.  Return 0 on success; any
+ * other value aborts the sweep. */
 typedef int (*slide_grad_fn)(void *user, int32_t layer, void *const *replica_dev_ptrs,
                              slide_stream_t stream);
 

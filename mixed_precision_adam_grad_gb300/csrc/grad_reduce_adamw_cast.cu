@@ -414,7 +414,24 @@ __global__ void k_cast_bf16(const float *src, uint16_t *w, int64_t n)
         w[i] = __bfloat16_as_ushort(__float2bfloat16_rn(src[i]));
 }
 
+__global__ void k_fill_zero(uint4 *p, size_t n16)
+{
+    const size_t stride = (size_t)gridDim.x * blockDim.x;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += stride)
+        p[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
 }  // namespace
+
+cudaError_t launch_fill_zero(void *p, size_t bytes, cudaStream_t stream)
+{
+    const size_t n16 = bytes / 16;
+    if (n16 == 0)
+        return cudaSuccess;
+    const int dev_blocks = sm_count(0) * 8;
+    k_fill_zero<<<dev_blocks, kThreads, 0, stream>>>(reinterpret_cast<uint4 *>(p), n16);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_cast_bf16(const float *src, uint16_t *w, int64_t n, cudaStream_t stream)
 {

@@ -48,4 +48,8 @@ cudaError_t launch_grad_reduce_adamw_cast(const ReplicaPtrs &g, int R, int64_t n
 // w[i] = bf16_rne(src[i]) (used when a caller overwrites a master copy).
 cudaError_t launch_cast_bf16(const float *src, uint16_t *w, int64_t n, cudaStream_t stream);
 
+// Zero `bytes` (a multiple of 16, 16-byte aligned) of device-accessible memory
+// (device memory, or pinned host memory through its device address).
+cudaError_t launch_fill_zero(void *p, size_t bytes, cudaStream_t stream);
+
 }  // namespace slide

@@ -1,0 +1,258 @@
+"""GPU tests of the host-resident streamed step (slide_model_step_streamed).
+
+A toy model of units of mixed sizes (including an empty one) runs with a tiny
+copy chunk so the slot handoff between the copy-out of one unit and the
+copy-in of the next happens over many chunks; every element is compared with
+the oracle after each step.  The invariants of synchronous data parallelism
+are checked: one update per unit per step (every t moves by exactly one),
+same version on entry (SLIDE_ERR_VERSION otherwise), and a sweep that stops
+part-way leaves the state marked until a common version is restored.
+Failures are made on the host (a callback that returns an error, a wait
+limit shorter than the work); no GPU fault, trap or hang is involved.
+"""
+import ctypes as C
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import oracle  # noqa: E402
+import synth  # noqa: E402
+from synth import workloads as W  # noqa: E402
+import parity_util as pu  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def S():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import mixed_precision_adam_grad_gb300 as S
+    return S
+
+
+class ModelGradsHolder:
+    """synth.ModelGrads with its arrays kept alive."""
+
+    def __init__(self, w: W.Workload, step: int):
+        self.numel = (C.c_int64 * len(w.units))(*[u.numel for u in w.units])
+        segs_b, offs, lens, scs = [0], [], [], []
+        for ui, u in enumerate(w.units):
+            for (off, n), sc in zip(u.segments(), w.tensor_scales(ui)):
+                offs.append(off)
+                lens.append(n)
+                scs.append(sc)
+            segs_b.append(len(offs))
+        self.seg_begin = (C.c_int32 * len(segs_b))(*segs_b)
+        self.seg_off = (C.c_int64 * len(offs))(*offs)
+        self.seg_len = (C.c_int64 * len(lens))(*lens)
+        self.seg_scale = (C.c_float * len(scs))(*scs)
+        self.mg = synth.ModelGrads(synth.spec(w.seed, w.grad_kind, w.zero_prob), len(w.units), w.R, step, 0,
+                                   C.cast(self.numel, C.c_void_p), C.cast(self.seg_begin, C.c_void_p),
+                                   C.cast(self.seg_off, C.c_void_p), C.cast(self.seg_len, C.c_void_p),
+                                   C.cast(self.seg_scale, C.c_void_p), w.grad_scale)
+
+
+def init_streamed(S, w, st):
+    """Seeded master in the pinned host state (written by the GPU through the
+    memory's device address), m = v = 0, BF16 copy = bf16(master)."""
+    for ui, u in enumerate(w.units):
+        th = synth.master(u.numel, w.seed, unit=ui)
+        S.slide_layer_set(st, ui, master=th, step=0)
+
+
+def toy(R=3, clip=0.0, seed=5):
+    sizes = [5000, 70001, (1 << 20) + 3, 0, 777, 123457]
+    return W.Workload("toy", [W.Unit(f"u{i}", [("a", n // 2), ("b", n - n // 2)]) for i, n in enumerate(sizes)],
+                      R=R, steps=3, seed=seed, max_grad_norm=clip, lr=1e-3, streamed=True)
+
+
+@pytest.mark.parametrize("clip,chunk", [(0.0, 64 << 10), (0.5, 256), (1e4, 1 << 20)])
+def test_streamed_toy_every_element(S, clip, chunk):
+    w = toy(clip=clip)
+    st = S.slide_state_create([u.numel for u in w.units], w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED,
+                              chunk_bytes=chunk)
+    try:
+        init_streamed(S, w, st)
+        ref = []
+        for ui, u in enumerate(w.units):
+            ref.append([synth.master(u.numel, w.seed, unit=ui), np.zeros(u.numel, np.float32),
+                        np.zeros(u.numel, np.float32), np.zeros(u.numel, np.uint16)])
+        hp = S.hparams(*w.hparams_tuple())
+        hp_or = pu.hp_oracle(w)
+        for t in range(1, w.steps + 1):
+            holder = ModelGradsHolder(w, t)
+            S.slide_model_step_streamed(st, synth.grad_fn_address(), holder.mg, hp)
+            for ui, u in enumerate(w.units):
+                reps = [pu.unit_grad_host(w, ui, t, r) for r in range(w.R)]
+                oracle.layer_step(reps, *ref[ui], hp_or, t)
+                a, b, c = (np.empty(u.numel, np.float32) for _ in range(3))
+                wb = np.empty(u.numel, np.uint16)
+                assert S.slide_layer_get(st, ui, a, b, c, wb) == t
+                rep = [pu.compare_fp32("theta", a, ref[ui][0]), pu.compare_fp32("m", b, ref[ui][1]),
+                       pu.compare_fp32("v", c, ref[ui][2]), pu.compare_bf16("w", wb, ref[ui][3])]
+                pu.assert_parity(rep)
+                # the host mirror that the next forward sweep delivers is bf16(master)
+                assert np.array_equal(wb, oracle.f32_to_bf16(a))
+                if clip == 0.0:
+                    assert all(r["not_bit_equal"] == 0 for r in rep[:3]), rep
+    finally:
+        S.slide_state_destroy(st)
+
+
+def test_streamed_python_callback_sees_master_and_errors_abort(S):
+    """A Python callback (ctypes) receives R writable replica buffers plus the
+    unit's FP32 master in the window; returning non-zero at one unit aborts
+    the sweep: units already written back carry the new version, the rest the
+    old one, and the state refuses further steps until restored."""
+    sizes = [1000, 2000, 3000, 4000]
+    R = 2
+    st = S.slide_state_create(sizes, R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED, chunk_bytes=4096)
+    seen = []
+
+    def cb(user, layer, ptrs, stream):
+        n = sizes[layer]
+        seen.append((layer, ptrs[R] is not None))
+        for r in range(R):  # zero gradients: the generator with scale 0
+            synth.dev_grad(ptrs[r], n, synth.spec(1), layer, 1, r, 0.0, stream=stream or 0)
+        return 7 if (fail_at[0] is not None and layer == fail_at[0]) else 0
+
+    fail_at = [None]
+    fn = S.SLIDE_GRAD_FN(cb)
+    try:
+        for ui, n in enumerate(sizes):
+            S.slide_layer_set(st, ui, master=np.full(n, 0.5, np.float32), step=0)
+        S.slide_model_step_streamed(st, fn, None, S.hparams())
+        assert [l for l, _ in seen] == [3, 2, 1, 0] and all(has for _, has in seen)
+        assert [S.slide_layer_get(st, i) for i in range(4)] == [1, 1, 1, 1]
+        fail_at[0] = 1
+        with pytest.raises(S.SlideError) as e:
+            S.slide_model_step_streamed(st, fn, None, S.hparams())
+        assert e.value.status == S.SLIDE_ERR_ABORTED
+        # reverse sweep order 3, 2, 1: units 3 and 2 were updated, 1 and 0 not
+        assert [S.slide_layer_get(st, i) for i in range(4)] == [1, 1, 2, 2]
+        fail_at[0] = None
+        with pytest.raises(S.SlideError) as e:
+            S.slide_model_step_streamed(st, fn, None, S.hparams())
+        assert e.value.status == S.SLIDE_ERR_ABORTED
+        for ui, n in enumerate(sizes):
+            S.slide_layer_set(st, ui, master=np.full(n, 0.5, np.float32), step=4)
+        S.slide_model_step_streamed(st, fn, None, S.hparams())
+        assert [S.slide_layer_get(st, i) for i in range(4)] == [5, 5, 5, 5]
+    finally:
+        S.slide_state_destroy(st)
+
+
+def test_streamed_version_gate(S):
+    sizes = [100, 200]
+    st = S.slide_state_create(sizes, 1, residency=S.SLIDE_RESIDENCY_HOST_STREAMED)
+    try:
+        S.slide_layer_set(st, 1, step=3)
+        w = W.Workload("v", [W.Unit("a", [("a", 100)]), W.Unit("b", [("b", 200)])], R=1, steps=1, seed=1)
+        holder = ModelGradsHolder(w, 1)
+        with pytest.raises(S.SlideError) as e:
+            S.slide_model_step_streamed(st, synth.grad_fn_address(), holder.mg, S.hparams())
+        assert e.value.status == S.SLIDE_ERR_VERSION
+        # slide_layer_step is for the HBM residency only
+        g = torch.zeros(128, dtype=torch.bfloat16, device="cuda")
+        with pytest.raises(S.SlideError) as e:
+            S.slide_layer_step(st, 0, [g], S.hparams())
+        assert e.value.status == S.SLIDE_ERR_STATE
+    finally:
+        S.slide_state_destroy(st)
+
+
+def test_streamed_wait_limit_returns_timeout(S):
+    """A wait limit (1 ms) far shorter than the sweep: the host wait gives up
+    with SLIDE_ERR_TIMEOUT while the GPU finishes normally; destroy then
+    waits for the streams and the context stays usable."""
+    sizes = [64 << 20, 64 << 20]
+    R = 4
+    st = S.slide_state_create(sizes, R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED, timeout_ms=1)
+    try:
+        w = W.Workload("to", [W.Unit("a", [("a", sizes[0])]), W.Unit("b", [("b", sizes[1])])], R=R, steps=1,
+                       seed=2)
+        holder = ModelGradsHolder(w, 1)
+        with pytest.raises(S.SlideError) as e:
+            S.slide_model_step_streamed(st, synth.grad_fn_address(), holder.mg, S.hparams())
+        assert e.value.status == S.SLIDE_ERR_TIMEOUT
+    finally:
+        S.slide_state_destroy(st)
+    x = torch.ones(1000, device="cuda")
+    assert float(x.sum()) == 1000.0
+
+
+def test_streamed_accounting_matches_allocation(S):
+    """Pinned host bytes = master+m+v+BF16 copy of every unit (14 B/param plus
+    256-byte alignment); the HBM window depends only on the largest unit."""
+    sizes = [3_000_000, 5_000_000, 1_000]
+    R = 4
+    dev_b, host_b = S.slide_state_bytes(sizes, R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED)
+    N = sum(sizes)
+    assert 14 * N <= host_b <= 14 * N + 4 * 256 * len(sizes)
+    dev_b2, _ = S.slide_state_bytes(sizes + [5_000_000] * 7, R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED)
+    assert dev_b2 == dev_b
+    free0, _ = torch.cuda.mem_get_info()
+    st = S.slide_state_create(sizes, R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED)
+    try:
+        free1, _ = torch.cuda.mem_get_info()
+        assert dev_b <= free0 - free1 <= dev_b + (64 << 20)
+    finally:
+        S.slide_state_destroy(st)
+
+
+def _mem_available():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+@pytest.mark.parametrize("cfg", [5, 4])
+def test_streamed_full_size_sampled(S, cfg):
+    """The full host-streamed workloads, sampled: every unit's sampled
+    elements against the oracle after each step; the mirror equals bf16 of
+    the master; t advanced once per step."""
+    w = W.ALL[cfg]()
+    sizes = [u.numel for u in w.units]
+    _, host_b = S.slide_state_bytes(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED)
+    if _mem_available() < host_b + (24 << 30):
+        pytest.skip(f"host memory: needs {host_b / 2**30:.0f} GiB pinned + 24 GiB headroom, "
+                    f"{_mem_available() / 2**30:.0f} GiB available")
+    st = S.slide_state_create(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED)
+    try:
+        for ui, u in enumerate(w.units):
+            th_p = S.slide_layer_ptrs(st, ui)[0]
+            synth.dev_master(th_p, u.numel, w.seed, unit=ui)
+        torch.cuda.synchronize()
+        check_units = sorted({0, len(w.units) // 2, len(w.units) - 1})
+        samples = {}
+        for ui in check_units:
+            u = w.units[ui]
+            idx = pu.sample_indices(u.numel, 50_000, seed=ui)
+            samples[ui] = [idx, synth.gather_master(idx, w.seed, unit=ui), np.zeros(idx.size, np.float32),
+                           np.zeros(idx.size, np.float32)]
+        hp = S.hparams(*w.hparams_tuple())
+        for t in range(1, w.steps + 1):
+            holder = ModelGradsHolder(w, t)
+            S.slide_model_step_streamed(st, synth.grad_fn_address(), holder.mg, hp)
+        for ui in check_units:
+            idx, th, m, v = samples[ui]
+            wb = pu.oracle_sampled(w, ui, idx, 1, w.steps, th, m, v)
+            n = w.units[ui].numel
+            a, b, c = (np.empty(n, np.float32) for _ in range(3))
+            wg = np.empty(n, np.uint16)
+            assert S.slide_layer_get(st, ui, a, b, c, wg) == w.steps
+            rep = [pu.compare_fp32("theta", a[idx], th), pu.compare_fp32("m", b[idx], m),
+                   pu.compare_fp32("v", c[idx], v), pu.compare_bf16("w", wg[idx], wb)]
+            pu.assert_parity(rep)
+            assert all(r["not_bit_equal"] == 0 for r in rep)
+            assert np.array_equal(wg[idx], oracle.f32_to_bf16(a[idx]))
+        assert all(S.slide_layer_get(st, ui) == w.steps for ui in range(len(w.units)))
+    finally:
+        S.slide_state_destroy(st)
