@@ -45,6 +45,10 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--no-streamed", action="store_true",
+                    help="skip the host-streamed leg (8-layer h=8192 model, ~98 GB pinned host memory)")
+    ap.add_argument("--streamed-config", type=int, default=5, choices=[4, 5])
+    ap.add_argument("--streamed-steps", type=int, default=2)
     ap.add_argument("--batches", type=int, default=4,
                     help="pre-generated gradient batches cycled by the steps (1 for small profiling runs)")
     ap.add_argument("--soak-s", type=float, default=1.5,
@@ -104,31 +108,53 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
+        with open(self.path) as f:
+            out = self.parse(f.readlines())
+        os.unlink(self.path)
+        return out
+
+    @staticmethod
+    def parse(lines):
+        """Median SM clock, max clock and the throttle reasons seen in the
+        nvidia-smi CSV lines (fields as in FIELDS, no header, no units)."""
         sms, maxs, reasons, n = [], [], set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sms.append(float(parts[1]))
-                    maxs.append(float(parts[2]))
-                except ValueError:
-                    continue
-                n += 1
-                for name, val in zip(names, parts[5:9]):
-                    if val.lower() == "active":
-                        reasons.add(name)
-        os.unlink(self.path)
+        for line in lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sms.append(float(parts[1]))
+                maxs.append(float(parts[2]))
+            except ValueError:
+                continue
+            n += 1
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
         return {"sm_mhz": statistics.median(sms) if sms else None,
                 "sm_max_mhz": max(maxs) if maxs else None,
                 "reasons": sorted(reasons), "samples": n}
 
 
+def max_over_ranks(x: float, dist=None) -> float:
+    """The largest value of x over all ranks (identity without a process group)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def workload(cfg):
     from synth import workloads as W
     return W.ALL[cfg]()
+
+
+def workload_any(cfg):
+    return workload(cfg)
 
 
 # ------------------------------------------------------------ oracle ----
@@ -186,6 +212,119 @@ def run_reference(args):
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+# ----------------------------------------------------------- streamed ----
+
+def mem_available_bytes():
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return 0
+
+
+def link_probe(torch, nbytes=1 << 30, reps=20):
+    """Pinned host <-> device copy bandwidth (GB/s): each direction alone,
+    then both at once on two streams (per direction and aggregate); medians."""
+    h_src = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    h_dst = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d_dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    d_src = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def one(direction):
+        a, b = ev(), ev()
+        st = s1 if direction == "h2d" else s2
+        with torch.cuda.stream(st):
+            a.record(st)
+            if direction == "h2d":
+                d_dst.copy_(h_src, non_blocking=True)
+            else:
+                h_dst.copy_(d_src, non_blocking=True)
+            b.record(st)
+        torch.cuda.synchronize()
+        return nbytes / (a.elapsed_time(b) * 1e-3) / 1e9
+
+    def both():
+        a, b1, b2 = ev(), ev(), ev()
+        a.record(s1)
+        s2.wait_event(a)
+        with torch.cuda.stream(s1):
+            d_dst.copy_(h_src, non_blocking=True)
+            b1.record(s1)
+        with torch.cuda.stream(s2):
+            h_dst.copy_(d_src, non_blocking=True)
+            b2.record(s2)
+        torch.cuda.synchronize()
+        t1, t2 = a.elapsed_time(b1) * 1e-3, a.elapsed_time(b2) * 1e-3
+        return nbytes / t1 / 1e9, nbytes / t2 / 1e9, 2 * nbytes / max(t1, t2) / 1e9
+
+    for _ in range(2):
+        one("h2d"), one("d2h"), both()
+    h2d = statistics.median(one("h2d") for _ in range(reps))
+    d2h = statistics.median(one("d2h") for _ in range(reps))
+    bi = [both() for _ in range(reps)]
+    out = {"h2d_gbs": h2d, "d2h_gbs": d2h,
+           "h2d_concurrent_gbs": statistics.median(x[0] for x in bi),
+           "d2h_concurrent_gbs": statistics.median(x[1] for x in bi),
+           "bidir_gbs": statistics.median(x[2] for x in bi),
+           "probe": f"{nbytes >> 20} MiB pinned<->device cudaMemcpyAsync, {reps} reps, medians"}
+    del h_src, h_dst, d_dst, d_src
+    return out
+
+
+def run_streamed(args, S, torch, synth):
+    """Host-resident streamed step of a whole model: s/step against the
+    host-link roofline measured in the same run."""
+    import ctypes as C
+    w = workload_any(args.streamed_config)
+    sizes = [u.numel for u in w.units]
+    N = sum(sizes)
+    _, host_b = S.slide_state_bytes(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED)
+    need = host_b + (24 << 30)
+    if mem_available_bytes() < need:
+        return {"workload": w.name, "skipped": f"host memory: {host_b / 1e9:.1f} GB pinned + 24 GiB headroom "
+                                                f"needed, {mem_available_bytes() / 1e9:.1f} GB available"}
+    link = link_probe(torch)
+    t0 = time.time()
+    st = S.slide_state_create(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED)
+    create_s = time.time() - t0
+    try:
+        for ui, u in enumerate(w.units):
+            synth.dev_master(S.slide_layer_ptrs(st, ui)[0], u.numel, w.seed, unit=ui)
+        torch.cuda.synchronize()
+        numel = (C.c_int64 * len(sizes))(*sizes)
+        mg = synth.ModelGrads(synth.spec(w.seed, w.grad_kind, w.zero_prob), len(sizes), w.R, 1, 0,
+                              C.cast(numel, C.c_void_p), None, None, None, None, w.grad_scale)
+        hp = S.hparams(*w.hparams_tuple())
+        fn = synth.grad_fn_address()
+        S.slide_model_step_streamed(st, fn, mg, hp)          # warm-up step
+        times = []
+        for k in range(args.streamed_steps):
+            mg.step = 2 + k
+            t0 = time.perf_counter()
+            S.slide_model_step_streamed(st, fn, mg, hp)      # returns after the last write-back
+            times.append(time.perf_counter() - t0)
+        dev_b = S.slide_state_bytes(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED)[0]
+    finally:
+        S.slide_state_destroy(st)
+    s_step = statistics.mean(times)
+    G = 1e9
+    t_roof = (2 * N / (link["h2d_gbs"] * G)
+              + max(12 * N / (link["h2d_concurrent_gbs"] * G), 14 * N / (link["d2h_concurrent_gbs"] * G),
+                    26 * N / (link["bidir_gbs"] * G)))
+    return {"workload": w.name, "description": w.description, "params": N, "replicas": w.R,
+            "steps": args.streamed_steps, "s_per_step": s_step, "s_per_step_each": times,
+            "gparam_s": N / s_step / 1e9, "roofline_s": t_roof, "frac": t_roof / s_step,
+            "link_bytes_per_step": {"h2d": 14 * N, "d2h": 14 * N},
+            "achieved_link_gbs_each_way": 14 * N / s_step / 1e9,
+            "link": link, "host_pinned_gb": host_b / 1e9, "window_gb": dev_b / 1e9,
+            "create_s": create_s, "timing": "host wall clock around each synchronous model step"}
 
 
 # --------------------------------------------------------------- ours ----
@@ -272,10 +411,7 @@ def run_ours(args):
         ms_total = start.elapsed_time(stop)
         pre_ms = [e[0].elapsed_time(e[1]) for e in ev]
         upd_ms = [e[1].elapsed_time(e[2]) for e in ev]
-        if dist:
-            t = torch.tensor([ms_total], device="cuda", dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms_total = float(t.item())
+        ms_total = max_over_ranks(ms_total, dist)
 
         # end to end through the public API: pinned host replicas in, BF16 copy out
         e2e = None
@@ -308,14 +444,15 @@ def run_ours(args):
             e1.record(stream)
             torch.cuda.synchronize()
             ms_e2e = e0.elapsed_time(e1)
-            if dist:
-                t = torch.tensor([ms_e2e], device="cuda", dtype=torch.float64)
-                dist.all_reduce(t, op=dist.ReduceOp.MAX)
-                ms_e2e = float(t.item())
+            ms_e2e = max_over_ranks(ms_e2e, dist)
             e2e = {"value": n * Ke * world / (ms_e2e * 1e-3) / 1e9, "unit": UNIT,
                    "h2d_bytes_per_step": 2 * R * n, "d2h_bytes_per_step": 2 * n, "steps": Ke}
     finally:
         S.slide_state_destroy(st)
+
+    streamed = None
+    if not args.no_streamed and world == 1:
+        streamed = run_streamed(args, S, torch, synth)
 
     if rank != 0:
         if dist:
@@ -369,6 +506,7 @@ def run_ours(args):
         "clocks": clocks,
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "streamed": streamed,
     }
     print(json.dumps(line), flush=True)
     if dist:

@@ -191,12 +191,15 @@ SLIDE_API slide_status slide_layer_ptrs(slide_state *st, int32_t layer, float **
  * clip on (copied from the device; synchronous).  1.0 before any such step. */
 SLIDE_API slide_status slide_layer_last_clip_coef(slide_state *st, int32_t layer, float *coef);
 
-/* Non-finite check (SLIDE_FLAG_CHECK_FINITE): waits for the device, then
- * returns SLIDE_ERR_NONFINITE if a step of `layer` since the previous call saw
- * a NaN or Inf in its mean gradient (and clears that mark), else SLIDE_OK.
- * Without the flag it always returns SLIDE_OK.  The update itself is not
- * skipped: the caller decides what to do (for example restore with
- * slide_layer_set). */
+/* Status of the steps of `layer` since the previous call (HBM residency):
+ * waits for the device, reads and clears the layer's status word, and returns
+ *   SLIDE_ERR_TIMEOUT   if a bounded wait inside the update kernel's copy
+ *                       pipeline ran out (the step is incomplete; restore the
+ *                       layer with slide_layer_set);
+ *   SLIDE_ERR_NONFINITE with SLIDE_FLAG_CHECK_FINITE, if a mean gradient held
+ *                       a NaN or Inf (the update was applied: the caller
+ *                       decides, for example to restore with slide_layer_set);
+ *   SLIDE_OK            otherwise. */
 SLIDE_API slide_status slide_layer_status(slide_state *st, int32_t layer);
 
 /* Tracing: CUDA events (cudaEvent_t values, created by the caller) that every

@@ -264,3 +264,4 @@ def _event(e):
 def slide_trace_events(st: SlideState, prepass_start=None, update_start=None, update_stop=None) -> None:
     _check(_lib().slide_trace_events(C.c_void_p(st.handle), _event(prepass_start), _event(update_start),
                                   _event(update_stop)))
+

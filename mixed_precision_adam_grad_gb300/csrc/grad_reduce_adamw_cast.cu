@@ -9,10 +9,21 @@
 // cores onto the GPU and fused into one kernel.
 //
 // The step is elementwise and bandwidth-bound ((26 + 2R) bytes and ~20 FP32
-// operations per parameter), so no tensor cores: each thread moves 16-byte
-// vectors (8 parameters) of every stream, the grid is persistent (SM count x
-// resident blocks) with a grid-stride loop, and UNROLL vectors per thread are
-// loaded before any is used to keep enough bytes in flight.
+// operations per parameter), so no tensor cores.  The kernel is a persistent
+// producer/consumer pipeline, one CTA per SM:
+//  - one producer thread streams tiles of kTile parameters of every input
+//    (R replicas, master, m, v) into a kStages-deep shared-memory ring with
+//    1-D bulk copies (cp.async.bulk, the TMA engine's linear mode), each
+//    stage guarded by a pair of mbarriers (full: bytes landed; empty: the
+//    consumers are done with it);
+//  - 8 consumer warps read a stage from shared memory, compute, release the
+//    stage, and write master, m, v and the BF16 copy straight to global
+//    memory with streaming stores.
+// The copies keep the loads in flight without registers, so a handful of
+// warps saturate HBM while the divisions and square roots run.  Tiles go to
+// CTAs round-robin (consecutive CTAs read consecutive addresses).  The part
+// of the layer after the last whole tile is done with plain vector loads by
+// one CTA, and the last n % 4 parameters with scalar accesses.
 //
 // Arithmetic: one IEEE FP32 operation per line of the update, explicit
 // __f*_rn intrinsics so nothing is contracted into an FMA, IEEE sqrt and
@@ -26,6 +37,10 @@
 // double-precision partial per block; the fused kernel turns the partials
 // into the coefficient in its prologue, in the same fixed order in every
 // block, so every block uses the same bits.
+//
+// Every wait on an mbarrier is bounded (kWaitLimitNs of wall time); a wait
+// that runs out sets bit 1 of the status word, waits (bounded) for the bulk
+// copies it issued to land, and the kernel returns.
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -35,14 +50,23 @@
 namespace slide {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;            // register-path kernels
+constexpr int kTile = 2048;              // parameters per pipeline tile
+constexpr int kStages = 2;               // shared-memory ring depth
+constexpr int kConsumerWarps = 8;        // kTile = 256 consumer threads x 8 parameters
+constexpr int kPipeThreads = (kConsumerWarps + 1) * 32;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+static_assert(kTile == kConsumerWarps * 32 * 8, "each consumer thread owns 8 parameters of a tile");
+
+constexpr unsigned kStatusNonFinite = 1u;
+constexpr unsigned kStatusWaitLimit = 2u;
 
 struct KArgs {
     ReplicaPtrs g;
-    float4 *theta;
-    float4 *m;
-    float4 *v;
-    uint4 *w;
+    float *theta;
+    float *m;
+    float *v;
+    uint16_t *w;
     int64_t n;
     AdamScalars s;
     const double *partials;
@@ -100,8 +124,45 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint16_t lo, uint16_t hi)
     return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
+// Mean gradient of parameter e (0..3) of a 4-wide group, from R 8-byte words.
+template <int R, bool CLIP, bool CHECK>
+__device__ __forceinline__ float mean_of(const uint2 (&gw)[R], int e, float coef, bool &bad)
+{
+    float x[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const uint32_t word = (e < 2) ? gw[r].x : gw[r].y;
+        x[r] = (e & 1) ? bf16_hi(word) : bf16_lo(word);
+    }
+    float g = replica_mean<R>(x);
+    if constexpr (CHECK)
+        bad |= !isfinite(g);
+    if constexpr (CLIP)
+        g = __fmul_rn(g, coef);
+    return g;
+}
+
+// Update 4 consecutive parameters held in registers and store them.
+template <int R, bool CLIP, bool CHECK>
+__device__ __forceinline__ void update4_store(const uint2 (&gw)[R], float4 th, float4 mm, float4 vv, int64_t e0,
+                                              const KArgs &a, const AdamScalars &s, float coef, bool &bad)
+{
+    float t[4] = {th.x, th.y, th.z, th.w};
+    float m[4] = {mm.x, mm.y, mm.z, mm.w};
+    float v[4] = {vv.x, vv.y, vv.z, vv.w};
+    uint16_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+        adamw_one(mean_of<R, CLIP, CHECK>(gw, e, coef, bad), t[e], m[e], v[e], w[e], s);
+    __stcs(reinterpret_cast<float4 *>(a.theta + e0), make_float4(t[0], t[1], t[2], t[3]));
+    __stcs(reinterpret_cast<float4 *>(a.m + e0), make_float4(m[0], m[1], m[2], m[3]));
+    __stcs(reinterpret_cast<float4 *>(a.v + e0), make_float4(v[0], v[1], v[2], v[3]));
+    __stcs(reinterpret_cast<uint2 *>(a.w + e0), make_uint2(pack_bf16x2(w[0], w[1]), pack_bf16x2(w[2], w[3])));
+}
+
 // Deterministic clip coefficient from the per-block partials: warp 0 sums
 // lane-strided in double, then a fixed shuffle-down tree; lane 0's result.
+// Called by every thread of the block.
 __device__ __forceinline__ float clip_coef_from_partials(const double *partials, int n_partials,
                                                           float max_norm)
 {
@@ -125,106 +186,231 @@ __device__ __forceinline__ float clip_coef_from_partials(const double *partials,
     return s_coef;
 }
 
-template <int R, bool CLIP, bool CHECK, int UNROLL>
-__global__ void __launch_bounds__(kThreads) k_grad_reduce_adamw_cast(KArgs a)
+// ---- mbarrier and bulk-copy helpers (inline PTX) ---------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n"
+        " .reg .pred p;\n"
+        " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait until the phase of `bar` with the given parity has completed; false if
+// kWaitLimitNs of wall time passed first.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity))
+                return true;
+        if (global_ns() - t0 > kWaitLimitNs)
+            return false;
+    }
+}
+
+// 1-D bulk copy global -> shared, completing `bytes` on the mbarrier.
+__device__ __forceinline__ void bulk_load(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst_smem)),
+        "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+template <int R>
+struct Pipe {
+    static constexpr uint32_t kGradBytes = kTile * 2;
+    static constexpr uint32_t kF32Bytes = kTile * 4;
+    static constexpr uint32_t kStageBytes = R * kGradBytes + 3 * kF32Bytes;
+    static constexpr uint32_t kSmemBytes = kStages * kStageBytes + 2 * kStages * 8;
+};
+
+template <int R, bool CLIP, bool CHECK>
+__global__ void __launch_bounds__(kPipeThreads, 1) k_grad_reduce_adamw_cast(KArgs a)
+{
+    using P = Pipe<R>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * P::kStageBytes);
+    uint64_t *empty = full + kStages;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kConsumerWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
     float coef = 1.0f;
     if constexpr (CLIP) {
-        coef = clip_coef_from_partials(a.partials, a.n_partials, a.max_norm);
+        coef = clip_coef_from_partials(a.partials, a.n_partials, a.max_norm);  // includes __syncthreads
         if (blockIdx.x == 0 && threadIdx.x == 0 && a.coef_out)
             *a.coef_out = coef;
+    } else {
+        __syncthreads();
     }
+    const int64_t ntiles = a.n / kTile;
+
+    if (warp == kConsumerWarps) {
+        // ---- producer: one thread issues the bulk copies of each tile ----
+        if (lane != 0)
+            return;
+        int stage = 0;
+        uint32_t phase = 0;
+        int issued[kStages];
+        uint32_t issued_phase[kStages];
+#pragma unroll
+        for (int i = 0; i < kStages; ++i)
+            issued[i] = 0, issued_phase[i] = 0;
+        bool ok = true;
+        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u)) {
+                ok = false;
+                break;
+            }
+            unsigned char *base = smem + stage * P::kStageBytes;
+            mbar_arrive_expect_tx(&full[stage], P::kStageBytes);
+            const int64_t e0 = tile * kTile;
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+                bulk_load(base + r * P::kGradBytes, static_cast<const uint16_t *>(a.g.p[r]) + e0, P::kGradBytes,
+                          &full[stage]);
+            bulk_load(base + R * P::kGradBytes, a.theta + e0, P::kF32Bytes, &full[stage]);
+            bulk_load(base + R * P::kGradBytes + P::kF32Bytes, a.m + e0, P::kF32Bytes, &full[stage]);
+            bulk_load(base + R * P::kGradBytes + 2 * P::kF32Bytes, a.v + e0, P::kF32Bytes, &full[stage]);
+            issued[stage] = 1;
+            issued_phase[stage] = phase;
+            if (++stage == kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        // No copy may still be landing in shared memory when the block ends:
+        // wait (bounded) for the last fill of every stage.
+        for (int i = 0; i < kStages; ++i)
+            if (issued[i] && !mbar_wait(&full[i], issued_phase[i]))
+                ok = false;
+        if (!ok && a.status)
+            atomicOr(a.status, kStatusWaitLimit);
+        return;
+    }
+
+    // ---- consumers: thread c owns parameters [4c, 4c+4) and [kTile/2 + 4c, +4) ----
     const AdamScalars s = a.s;
-    const int64_t nvec = a.n >> 3;
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
-    const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
+    const int c = threadIdx.x;
     bool bad = false;
-
-    for (int64_t k0 = tid; k0 < nvec; k0 += stride * UNROLL) {
-        uint4 gv[UNROLL][R];
-        float4 th[UNROLL][2], mv[UNROLL][2], vv[UNROLL][2];
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
-            const int64_t k = k0 + (int64_t)u * stride;
-            if (k < nvec) {
-#pragma unroll
-                for (int r = 0; r < R; ++r)
-                    gv[u][r] = __ldcs(reinterpret_cast<const uint4 *>(a.g.p[r]) + k);
-                th[u][0] = __ldcs(a.theta + 2 * k);
-                th[u][1] = __ldcs(a.theta + 2 * k + 1);
-                mv[u][0] = __ldcs(a.m + 2 * k);
-                mv[u][1] = __ldcs(a.m + 2 * k + 1);
-                vv[u][0] = __ldcs(a.v + 2 * k);
-                vv[u][1] = __ldcs(a.v + 2 * k + 1);
-            }
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        if (!mbar_wait(&full[stage], phase)) {
+            if (a.status)
+                atomicOr(a.status, kStatusWaitLimit);
+            break;
         }
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
-            const int64_t k = k0 + (int64_t)u * stride;
-            if (k < nvec) {
-                float tt[8] = {th[u][0].x, th[u][0].y, th[u][0].z, th[u][0].w,
-                               th[u][1].x, th[u][1].y, th[u][1].z, th[u][1].w};
-                float mm[8] = {mv[u][0].x, mv[u][0].y, mv[u][0].z, mv[u][0].w,
-                               mv[u][1].x, mv[u][1].y, mv[u][1].z, mv[u][1].w};
-                float vq[8] = {vv[u][0].x, vv[u][0].y, vv[u][0].z, vv[u][0].w,
-                               vv[u][1].x, vv[u][1].y, vv[u][1].z, vv[u][1].w};
-                uint16_t ww[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    float x[R];
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const uint32_t word = (&gv[u][r].x)[e >> 1];
-                        x[r] = (e & 1) ? bf16_hi(word) : bf16_lo(word);
-                    }
-                    float g = replica_mean<R>(x);
-                    if constexpr (CHECK)
-                        bad |= !isfinite(g);
-                    if constexpr (CLIP)
-                        g = __fmul_rn(g, coef);
-                    adamw_one(g, tt[e], mm[e], vq[e], ww[e], s);
-                }
-                __stcs(a.theta + 2 * k, make_float4(tt[0], tt[1], tt[2], tt[3]));
-                __stcs(a.theta + 2 * k + 1, make_float4(tt[4], tt[5], tt[6], tt[7]));
-                __stcs(a.m + 2 * k, make_float4(mm[0], mm[1], mm[2], mm[3]));
-                __stcs(a.m + 2 * k + 1, make_float4(mm[4], mm[5], mm[6], mm[7]));
-                __stcs(a.v + 2 * k, make_float4(vq[0], vq[1], vq[2], vq[3]));
-                __stcs(a.v + 2 * k + 1, make_float4(vq[4], vq[5], vq[6], vq[7]));
-                __stcs(a.w + k, make_uint4(pack_bf16x2(ww[0], ww[1]), pack_bf16x2(ww[2], ww[3]),
-                                           pack_bf16x2(ww[4], ww[5]), pack_bf16x2(ww[6], ww[7])));
-            }
-        }
-    }
-
-    // Ragged tail: the last n % 8 parameters, one per thread, scalar accesses.
-    const int64_t tail0 = nvec << 3;
-    if (tid < a.n - tail0) {
-        const int64_t i = tail0 + tid;
-        float x[R];
+        const unsigned char *base = smem + stage * P::kStageBytes;
+        uint2 g0[R], g1[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
-            const uint16_t h = reinterpret_cast<const uint16_t *>(a.g.p[r])[i];
-            x[r] = __uint_as_float((uint32_t)h << 16);
+            const unsigned char *gb = base + r * P::kGradBytes;
+            g0[r] = *reinterpret_cast<const uint2 *>(gb + c * 8);
+            g1[r] = *reinterpret_cast<const uint2 *>(gb + kTile + c * 8);
         }
-        float g = replica_mean<R>(x);
-        if constexpr (CHECK)
-            bad |= !isfinite(g);
-        if constexpr (CLIP)
-            g = __fmul_rn(g, coef);
-        float *thp = reinterpret_cast<float *>(a.theta);
-        float *mp = reinterpret_cast<float *>(a.m);
-        float *vp = reinterpret_cast<float *>(a.v);
-        float t = thp[i], mm = mp[i], vq = vp[i];
-        uint16_t ww;
-        adamw_one(g, t, mm, vq, ww, s);
-        thp[i] = t;
-        mp[i] = mm;
-        vp[i] = vq;
-        reinterpret_cast<uint16_t *>(a.w)[i] = ww;
+        const unsigned char *fb = base + R * P::kGradBytes;
+        const float4 t0 = *reinterpret_cast<const float4 *>(fb + c * 16);
+        const float4 t1 = *reinterpret_cast<const float4 *>(fb + kTile * 2 + c * 16);
+        const float4 m0 = *reinterpret_cast<const float4 *>(fb + P::kF32Bytes + c * 16);
+        const float4 m1 = *reinterpret_cast<const float4 *>(fb + P::kF32Bytes + kTile * 2 + c * 16);
+        const float4 v0 = *reinterpret_cast<const float4 *>(fb + 2 * P::kF32Bytes + c * 16);
+        const float4 v1 = *reinterpret_cast<const float4 *>(fb + 2 * P::kF32Bytes + kTile * 2 + c * 16);
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(&empty[stage]);
+        const int64_t e0 = tile * kTile + 4 * c;
+        update4_store<R, CLIP, CHECK>(g0, t0, m0, v0, e0, a, s, coef, bad);
+        update4_store<R, CLIP, CHECK>(g1, t1, m1, v1, e0 + kTile / 2, a, s, coef, bad);
+        if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+        }
+    }
+
+    // ---- the part after the last whole tile, by one CTA, plain loads ----
+    if (blockIdx.x == (unsigned)(ntiles % gridDim.x)) {
+        const int64_t base_e = ntiles * kTile;
+        const int64_t rem = a.n - base_e;           // < kTile
+        const int64_t groups = rem >> 2;            // 4-wide groups, < 512
+        for (int64_t q = c; q < groups; q += kConsumerWarps * 32) {
+            const int64_t e0 = base_e + 4 * q;
+            uint2 gw[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+                gw[r] = __ldcs(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.g.p[r]) + e0));
+            const float4 t = __ldcs(reinterpret_cast<const float4 *>(a.theta + e0));
+            const float4 m = __ldcs(reinterpret_cast<const float4 *>(a.m + e0));
+            const float4 v = __ldcs(reinterpret_cast<const float4 *>(a.v + e0));
+            update4_store<R, CLIP, CHECK>(gw, t, m, v, e0, a, s, coef, bad);
+        }
+        const int64_t tail0 = base_e + (groups << 2);
+        if (c < a.n - tail0) {
+            const int64_t i = tail0 + c;
+            float x[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+                x[r] = __uint_as_float((uint32_t)static_cast<const uint16_t *>(a.g.p[r])[i] << 16);
+            float g = replica_mean<R>(x);
+            if constexpr (CHECK)
+                bad |= !isfinite(g);
+            if constexpr (CLIP)
+                g = __fmul_rn(g, coef);
+            float t = a.theta[i], m = a.m[i], v = a.v[i];
+            uint16_t w;
+            adamw_one(g, t, m, v, w, s);
+            a.theta[i] = t;
+            a.m[i] = m;
+            a.v[i] = v;
+            a.w[i] = w;
+        }
     }
     if constexpr (CHECK) {
         if (bad && a.status)
-            atomicOr(a.status, 1u);
+            atomicOr(a.status, kStatusNonFinite);
     }
 }
 
@@ -330,7 +516,21 @@ __global__ void __launch_bounds__(kThreads) k_grad_sqnorm(SqArgs a)
     }
 }
 
-// Resident blocks per SM of a kernel, cached per (kernel, device).
+int sm_count(int device)
+{
+    static int cache[64] = {0};
+    if (device < 0 || device >= 64)
+        return 1;
+    if (cache[device] == 0) {
+        int c = 0;
+        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || c < 1)
+            c = 1;
+        cache[device] = c;
+    }
+    return cache[device];
+}
+
+// Resident blocks per SM of a register-path kernel, cached per (kernel, device).
 template <auto Kernel>
 int blocks_per_sm(int device)
 {
@@ -346,21 +546,8 @@ int blocks_per_sm(int device)
     return cache[device];
 }
 
-int sm_count(int device)
-{
-    static int cache[64] = {0};
-    if (device < 0 || device >= 64)
-        return 1;
-    if (cache[device] == 0) {
-        int c = 0;
-        if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || c < 1)
-            c = 1;
-        cache[device] = c;
-    }
-    return cache[device];
-}
-
-// Persistent grid: SMs x resident blocks, fewer if there is less work.
+// Persistent grid for a register-path kernel: SMs x resident blocks, fewer
+// if there is less work.
 template <auto Kernel>
 unsigned grid_for(int device, int64_t n, int cap)
 {
@@ -375,15 +562,26 @@ unsigned grid_for(int device, int64_t n, int cap)
     return (unsigned)g;
 }
 
-constexpr int kUnrollStep = 2;
 constexpr int kUnrollSq = 2;
 
 template <int R, bool CLIP, bool CHECK>
 cudaError_t launch_step_r(const KArgs &a, int device, cudaStream_t stream)
 {
-    constexpr auto kern = k_grad_reduce_adamw_cast<R, CLIP, CHECK, kUnrollStep>;
-    unsigned grid = grid_for<kern>(device, a.n, 1 << 30);
-    kern<<<grid, kThreads, 0, stream>>>(a);
+    constexpr auto kern = k_grad_reduce_adamw_cast<R, CLIP, CHECK>;
+    constexpr uint32_t smem = Pipe<R>::kSmemBytes;
+    static int attr_set[64] = {0};
+    if (device >= 0 && device < 64 && !attr_set[device]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess)
+            return e;
+        attr_set[device] = 1;
+    }
+    // one CTA per SM, never more CTAs than whole tiles (at least one, for the tail)
+    int64_t grid = sm_count(device);
+    const int64_t ntiles = a.n / kTile;
+    if (grid > ntiles)
+        grid = ntiles > 0 ? ntiles : 1;
+    kern<<<(unsigned)grid, kPipeThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -466,13 +664,13 @@ cudaError_t launch_grad_reduce_adamw_cast(const ReplicaPtrs &g, int R, int64_t n
                                           const ClipScratch *clip, int n_partials, float max_norm,
                                           bool check_finite, int device, cudaStream_t stream)
 {
-    const bool do_clip = clip != nullptr && max_norm > 0.0f;
+    const bool do_clip = clip != nullptr && clip->partials != nullptr && max_norm > 0.0f;
     KArgs a{};
     a.g = g;
-    a.theta = reinterpret_cast<float4 *>(theta);
-    a.m = reinterpret_cast<float4 *>(m);
-    a.v = reinterpret_cast<float4 *>(v);
-    a.w = reinterpret_cast<uint4 *>(w);
+    a.theta = theta;
+    a.m = m;
+    a.v = v;
+    a.w = w;
     a.n = n;
     a.s = s;
     a.partials = do_clip ? clip->partials : nullptr;

@@ -336,8 +336,7 @@ slide_status slide_layer_step(slide_state *st, int32_t layer, const void *const 
         }
         if (st->trace[1])
             cudaEventRecord(st->trace[1], s);
-        e = launch_grad_reduce_adamw_cast(g, R, L.n, L.theta, L.m, L.v, w, sc,
-                                          (clip || check) ? &L.scratch : nullptr, n_partials,
+        e = launch_grad_reduce_adamw_cast(g, R, L.n, L.theta, L.m, L.v, w, sc, &L.scratch, n_partials,
                                           clip ? hp->max_grad_norm : 0.0f, check, st->device, s);
         if (e != cudaSuccess)
             return fail_cuda(e, "grad_reduce_adamw_cast launch");
@@ -385,8 +384,18 @@ slide_status slide_layer_set(slide_state *st, int32_t layer, const float *master
             return fail_cuda(e, "cudaMemcpy in slide_layer_set");
     }
     if (master && L.n > 0) {
-        // The pinned host arrays of the streamed residency are device-accessible too.
-        e = launch_cast_bf16(L.theta, L.w, L.n, 0);
+        // The pinned host arrays of the streamed residency are reached through
+        // their device addresses.
+        float *th_d = L.theta;
+        uint16_t *w_d = L.w;
+        if (st->cfg.residency == SLIDE_RESIDENCY_HOST_STREAMED) {
+            e = cudaHostGetDevicePointer((void **)&th_d, L.theta, 0);
+            if (e == cudaSuccess)
+                e = cudaHostGetDevicePointer((void **)&w_d, L.w, 0);
+            if (e != cudaSuccess)
+                return fail_cuda(e, "cudaHostGetDevicePointer in slide_layer_set");
+        }
+        e = launch_cast_bf16(th_d, w_d, L.n, 0);
         if (e == cudaSuccess)
             e = cudaDeviceSynchronize();
         if (e != cudaSuccess)
@@ -474,7 +483,7 @@ slide_status slide_layer_status(slide_state *st, int32_t layer)
     if (rc != SLIDE_OK)
         return rc;
     LayerState &L = st->layers[layer];
-    if (!(st->cfg.flags & SLIDE_FLAG_CHECK_FINITE) || !L.scratch.status)
+    if (!L.scratch.status)
         return SLIDE_OK;
     DeviceGuard guard(st->device);
     unsigned word = 0;
@@ -485,7 +494,9 @@ slide_status slide_layer_status(slide_state *st, int32_t layer)
         e = cudaMemset(L.scratch.status, 0, sizeof word);
     if (e != cudaSuccess)
         return fail_cuda(e, "reading the status word");
-    if (word & 1u)
+    if (word & 2u)
+        return fail(SLIDE_ERR_TIMEOUT, "a pipeline wait inside the kernel reached its limit; the step is incomplete");
+    if ((word & 1u) && (st->cfg.flags & SLIDE_FLAG_CHECK_FINITE))
         return fail(SLIDE_ERR_NONFINITE, "a non-finite mean gradient was seen");
     clear_error();
     return SLIDE_OK;

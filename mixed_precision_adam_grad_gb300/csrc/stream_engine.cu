@@ -336,9 +336,9 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
                 if (e != cudaSuccess)
                     break;
             }
-            e = launch_grad_reduce_adamw_cast(g, R, U.n, s.arr[0], s.arr[1], s.arr[2], s.w, sc,
-                                              (clip || check) ? &s.scratch : nullptr, n_partials,
-                                              clip ? hp.max_grad_norm : 0.0f, check, st->device, E->s_comp);
+            e = launch_grad_reduce_adamw_cast(g, R, U.n, s.arr[0], s.arr[1], s.arr[2], s.w, sc, &s.scratch,
+                                              n_partials, clip ? hp.max_grad_norm : 0.0f, check, st->device,
+                                              E->s_comp);
             if (e != cudaSuccess)
                 break;
         }
@@ -371,18 +371,22 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
     if (rc == SLIDE_OK && wrc != SLIDE_OK)
         rc = wrc;
 
+    unsigned word = 0;
+    if (wrc == SLIDE_OK) {
+        for (int k = 0; k < kSlots; ++k) {
+            unsigned w = 0;
+            if (cudaMemcpy(&w, E->slots[k].scratch.status, sizeof w, cudaMemcpyDeviceToHost) == cudaSuccess && w)
+                cudaMemset(E->slots[k].scratch.status, 0, sizeof w);
+            word |= w;
+        }
+        if ((word & 2u) && rc == SLIDE_OK)
+            rc = fail(SLIDE_ERR_TIMEOUT, "a pipeline wait inside the update kernel reached its limit");
+    }
     if (rc == SLIDE_OK) {
         for (LayerState &U : st->layers)
             U.t = t;
-        if (check) {
-            unsigned words[kSlots] = {0, 0};
-            for (int k = 0; k < kSlots; ++k) {
-                cudaMemcpy(&words[k], E->slots[k].scratch.status, sizeof(unsigned), cudaMemcpyDeviceToHost);
-                cudaMemset(E->slots[k].scratch.status, 0, sizeof(unsigned));
-            }
-            if ((words[0] | words[1]) & 1u)
-                return fail(SLIDE_ERR_NONFINITE, "a non-finite mean gradient was seen (the step was applied)");
-        }
+        if (check && (word & 1u))
+            return fail(SLIDE_ERR_NONFINITE, "a non-finite mean gradient was seen (the step was applied)");
         return SLIDE_OK;
     }
     // Aborted part-way: units whose write-back was enqueued and has completed

@@ -1,0 +1,117 @@
+"""Host-side tests of the C-ABI library (no GPU needed): it loads, exports every
+entry point include/slide.h declares, validates configurations before
+touching a device, and its byte accounting follows the 16N-byte state of
+mixed-precision Adam ("SlideDP: Scaling Host-Resident LLM Fine-Tuning Across
+Multiple GPUs", Prerequisites: BF16 weights 2N + BF16 gradients 2N + FP32
+master 4N + FP32 Adam moments 8N) and the 12 = 4 + 4 + 4 bytes of FP32 state
+per parameter ("Accelerating the Training of Large Language Models using
+Efficient Activation Rematerialization and Optimal Hybrid Parallelism",
+section 3, memory footprint item 2).
+"""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def S():
+    import __graft_entry__  # noqa: F401  (puts the repo root on sys.path)
+    from mixed_precision_adam_grad_gb300 import build
+    build.build()
+    import mixed_precision_adam_grad_gb300 as S
+    return S
+
+
+def declared_symbols():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            text = open(os.path.join(inc, f)).read()
+            names |= set(re.findall(r"SLIDE_API[^;(]*?\b(slide_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_symbol(S):
+    names = declared_symbols()
+    assert {"slide_state_create", "slide_layer_step", "slide_model_step_streamed",
+            "slide_state_destroy"} <= set(names), names
+    lib = C.CDLL(S.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    assert S.slide_abi_version() == 1
+
+
+def test_binding_fails_loudly_without_library(S, monkeypatch):
+    from mixed_precision_adam_grad_gb300 import _binding
+    monkeypatch.setattr(_binding, "LIB_PATH", os.path.join(ROOT, "no_such_libslide.so"))
+    with pytest.raises(ImportError):
+        _binding._load()
+
+
+A = 256
+
+
+def al(x):
+    return (x + A - 1) // A * A
+
+
+def test_accounting_16N(S):
+    """Per parameter the library holds 4 (master) + 4 + 4 (m, v) + 2 (BF16
+    copy) bytes; with the 2 bytes of one BF16 gradient that the caller holds
+    this is the pages' 16 bytes per parameter."""
+    sizes = [100_930_560, 1, 17, 0]
+    dev, host = S.slide_state_bytes(sizes, 4)
+    scratch = al(8 * 4096) + A
+    assert host == 0
+    assert dev == sum(3 * al(4 * n) + al(2 * n) for n in sizes) + len(sizes) * scratch
+    N = sum(sizes)
+    state_per_param = 4 + 4 + 4 + 2
+    assert state_per_param + 2 == 16              # + one BF16 gradient replica
+    assert 4 + 4 + 4 == 12                        # FP32 master + two Adam moments
+    assert state_per_param * N <= dev - len(sizes) * scratch <= state_per_param * N + 4 * A * len(sizes)
+
+
+def test_accounting_streamed_window_independent_of_N(S):
+    one = [330_311_680]
+    many = [778_567_680] + [330_311_680] * 40 + [778_567_680]
+    d1, h1 = S.slide_state_bytes([778_567_680] + one, 4, residency=S.SLIDE_RESIDENCY_HOST_STREAMED)
+    d2, h2 = S.slide_state_bytes(many, 4, residency=S.SLIDE_RESIDENCY_HOST_STREAMED)
+    assert d1 == d2                                    # window: two slots of the largest unit
+    N = sum(many)
+    assert N == 14_769_602_560
+    assert 14 * N <= h2 <= 14 * N + 4 * A * len(many)  # master, m, v, BF16 mirror
+    R, maxn = 4, 778_567_680
+    slot = 3 * al(4 * maxn) + al(2 * maxn) * (1 + R) + al(8 * 4096) + A
+    assert d2 == 2 * slot
+
+
+@pytest.mark.parametrize("kw,msg", [
+    (dict(layer_numel=[10], n_replicas=0), "n_replicas"),
+    (dict(layer_numel=[10], n_replicas=9), "n_replicas"),
+    (dict(layer_numel=[-1], n_replicas=1), "layer_numel"),
+    (dict(layer_numel=[10], n_replicas=1, residency=7), "residency"),
+    (dict(layer_numel=[10], n_replicas=1, chunk_bytes=100), "chunk_bytes"),
+    (dict(layer_numel=[10], n_replicas=1, window_layers=3), "window_layers"),
+    (dict(layer_numel=[10], n_replicas=1, flags=8), "flag"),
+    (dict(layer_numel=[], n_replicas=1), "n_layers"),
+])
+def test_config_validation_without_gpu(S, kw, msg):
+    numel = kw.pop("layer_numel")
+    R = kw.pop("n_replicas")
+    for fn in (S.slide_state_bytes, S.slide_state_create):
+        with pytest.raises(S.SlideError) as e:
+            fn(numel, R, **kw)
+        assert e.value.status == S.SLIDE_ERR_INVALID_ARG
+        assert msg in str(e.value)
+
+
+def test_null_state_is_rejected(S):
+    lib = S.lib
+    assert lib.slide_layer_status(None, 0) == S.SLIDE_ERR_INVALID_ARG
+    assert "NULL" in S.slide_last_error()
+    lib.slide_state_destroy(None)  # NULL-safe
