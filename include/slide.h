@@ -210,6 +210,33 @@ SLIDE_API slide_status slide_layer_status(slide_state *st, int32_t layer);
 SLIDE_API slide_status slide_trace_events(slide_state *st, void *ev_prepass_start,
                                           void *ev_update_start, void *ev_update_stop);
 
+/* The fused step for callers that cannot allocate GPU memory.  The paper has
+ * no counterpart to this entry point; it exists for code that may not call
+ * cudaMalloc (an allocator hook or host callback that must not re-enter the
+ * CUDA allocator, a process whose GPU memory pool is owned and capped by a
+ * framework, a runtime that forbids allocation after start-up) and so cannot
+ * hold a slide_state.
+ *   The caller owns every array: grad_replicas (host array of n_replicas
+ *   device pointers to n BF16 values each), master, m, v (n FP32 values each,
+ *   updated in place) and bf16_out (n BF16 values written); all device
+ *   pointers, 16-byte aligned.  step is the 1-based update count t of this
+ *   update (the caller keeps it).  Same arithmetic as slide_layer_step.
+ *   The clip's scratch (4096 per-block partial sums and the coefficient,
+ *   about 32 KiB) is a fixed array in the library's device memory, allocated
+ *   when the library is loaded on a GPU and held until the process exits; the
+ *   call allocates and frees nothing.  Limits: 0 <= n <= 2^40 and
+ *   1 <= n_replicas <= 8; anything else returns SLIDE_ERR_INVALID_ARG.
+ *   The first call on a device (with that device current) looks up the
+ *   scratch's device address with cudaGetSymbolAddress and caches it; make
+ *   that first call before any stream capture.  Every call shares the one
+ *   scratch, so calls that may overlap on the GPU (different streams, not
+ *   ordered) race with each other: order them.  Stream-ordered; returns before
+ *   the GPU finishes. */
+SLIDE_API slide_status slide_adamw_step_noalloc(int64_t n, int32_t n_replicas, const void *const *grad_replicas,
+                                                float *master, float *m, float *v, void *bf16_out,
+                                                const slide_adam_hparams *hp, int64_t step,
+                                                slide_stream_t stream);
+
 /* Message of the last error on this host thread ("" if none). */
 SLIDE_API const char *slide_last_error(void);
 

@@ -87,6 +87,9 @@ def _load():
     L.slide_layer_status.restype = S
     L.slide_trace_events.argtypes = [P, P, P, P]
     L.slide_trace_events.restype = S
+    L.slide_adamw_step_noalloc.argtypes = [C.c_int64, C.c_int32, C.POINTER(C.c_void_p), P, P, P, P,
+                                           C.POINTER(slide_adam_hparams), C.c_int64, P]
+    L.slide_adamw_step_noalloc.restype = S
     L.slide_last_error.argtypes = []
     L.slide_last_error.restype = C.c_char_p
     L.slide_abi_version.argtypes = []
@@ -265,3 +268,12 @@ def slide_trace_events(st: SlideState, prepass_start=None, update_start=None, up
     _check(_lib().slide_trace_events(C.c_void_p(st.handle), _event(prepass_start), _event(update_start),
                                   _event(update_stop)))
 
+
+def slide_adamw_step_noalloc(n: int, grad_replicas, master, m, v, bf16_out, hp: slide_adam_hparams,
+                             step: int, stream=None) -> None:
+    """The step for callers that cannot allocate GPU memory: the caller owns
+    every array and the 1-based step count; the library allocates nothing."""
+    ptrs = [_ptr(g) for g in grad_replicas]
+    arr = (C.c_void_p * max(1, len(ptrs)))(*ptrs)
+    _check(_lib().slide_adamw_step_noalloc(n, len(ptrs), arr, _ptr(master), _ptr(m), _ptr(v), _ptr(bf16_out),
+                                           C.byref(hp), step, _stream(stream)))
