@@ -216,6 +216,13 @@ def run_reference(args):
 
 # ----------------------------------------------------------- streamed ----
 
+def kernel_source_sha256():
+    import hashlib
+    p = os.path.join(ROOT, "mixed_precision_adam_grad_gb300", "csrc", "grad_reduce_adamw_cast.cu")
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
 def mem_available_bytes():
     try:
         with open("/proc/meminfo") as f:
@@ -280,17 +287,34 @@ def link_probe(torch, nbytes=1 << 30, reps=20):
 
 def run_streamed(args, S, torch, synth):
     """Host-resident streamed step of a whole model: s/step against the
-    host-link roofline measured in the same run."""
+    host-link roofline measured in the same run.  The gradient callback stands
+    in for the backward pass; in the timed steps it copies pre-generated
+    replicas (the workload's distribution) from a pool in HBM into the window,
+    so the time is the engine's copies and update; one more step with the
+    on-the-fly generator as the callback is reported beside it."""
     import ctypes as C
     w = workload_any(args.streamed_config)
     sizes = [u.numel for u in w.units]
     N = sum(sizes)
+    maxn = max(sizes)
     _, host_b = S.slide_state_bytes(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED)
     need = host_b + (24 << 30)
     if mem_available_bytes() < need:
         return {"workload": w.name, "skipped": f"host memory: {host_b / 1e9:.1f} GB pinned + 24 GiB headroom "
                                                 f"needed, {mem_available_bytes() / 1e9:.1f} GB available"}
     link = link_probe(torch)
+    n_pool = 2
+    sp = synth.spec(w.seed, w.grad_kind, w.zero_prob)
+    pool = [torch.empty(maxn + 64, dtype=torch.int16, device="cuda") for _ in range(n_pool * w.R)]
+    for k in range(n_pool):
+        for r in range(w.R):
+            synth.dev_grad(pool[k * w.R + r].data_ptr(), maxn, sp, 1000 + k, 0, r, w.grad_scale)
+    torch.cuda.synchronize()
+    numel = (C.c_int64 * len(sizes))(*sizes)
+    pool_ptrs = (C.c_void_p * len(pool))(*[t.data_ptr() for t in pool])
+    pg = synth.PoolGrads(w.R, n_pool, 0, 0, C.cast(numel, C.c_void_p), C.cast(pool_ptrs, C.c_void_p))
+    mg = synth.ModelGrads(sp, len(sizes), w.R, 1, 0, C.cast(numel, C.c_void_p), None, None, None, None,
+                          w.grad_scale)
     t0 = time.time()
     st = S.slide_state_create(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED)
     create_s = time.time() - t0
@@ -298,21 +322,22 @@ def run_streamed(args, S, torch, synth):
         for ui, u in enumerate(w.units):
             synth.dev_master(S.slide_layer_ptrs(st, ui)[0], u.numel, w.seed, unit=ui)
         torch.cuda.synchronize()
-        numel = (C.c_int64 * len(sizes))(*sizes)
-        mg = synth.ModelGrads(synth.spec(w.seed, w.grad_kind, w.zero_prob), len(sizes), w.R, 1, 0,
-                              C.cast(numel, C.c_void_p), None, None, None, None, w.grad_scale)
         hp = S.hparams(*w.hparams_tuple())
-        fn = synth.grad_fn_address()
-        S.slide_model_step_streamed(st, fn, mg, hp)          # warm-up step
+        fn_pool, fn_gen = synth.pool_grad_fn_address(), synth.grad_fn_address()
+        S.slide_model_step_streamed(st, fn_pool, pg, hp)          # warm-up step
         times = []
         for k in range(args.streamed_steps):
-            mg.step = 2 + k
+            pg.step = 1 + k
             t0 = time.perf_counter()
-            S.slide_model_step_streamed(st, fn, mg, hp)      # returns after the last write-back
+            S.slide_model_step_streamed(st, fn_pool, pg, hp)      # returns after the last write-back
             times.append(time.perf_counter() - t0)
+        t0 = time.perf_counter()
+        S.slide_model_step_streamed(st, fn_gen, mg, hp)
+        gen_s = time.perf_counter() - t0
         dev_b = S.slide_state_bytes(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED)[0]
     finally:
         S.slide_state_destroy(st)
+        del pool
     s_step = statistics.mean(times)
     G = 1e9
     t_roof = (2 * N / (link["h2d_gbs"] * G)
@@ -324,7 +349,11 @@ def run_streamed(args, S, torch, synth):
             "link_bytes_per_step": {"h2d": 14 * N, "d2h": 14 * N},
             "achieved_link_gbs_each_way": 14 * N / s_step / 1e9,
             "link": link, "host_pinned_gb": host_b / 1e9, "window_gb": dev_b / 1e9,
-            "create_s": create_s, "timing": "host wall clock around each synchronous model step"}
+            "create_s": create_s,
+            "grad_callback": f"copies pre-generated replicas ({n_pool} sets, the workload's distribution) "
+                             "from HBM into the window",
+            "s_per_step_with_generator_callback": gen_s,
+            "timing": "host wall clock around each synchronous model step"}
 
 
 # --------------------------------------------------------------- ours ----
@@ -477,11 +506,17 @@ def run_ours(args):
                "sample": f"first {min(n, 1 << 24)} parameters of the layer as a layer of their own, "
                          f"R={R}{', clip over the sample' if clip else ''}, {steps} steps "
                          f"({el:.1f} s of single-thread CPU time; inputs generated outside the timed calls)"}
-    traffic = None
+    traffic, traffic_note = None, "no ncu capture recorded for this workload"
     prof = os.path.join(ROOT, "profiles", f"traffic_{w.name}.json")
     if os.path.exists(prof):
         with open(prof) as f:
-            traffic = json.load(f).get("grad_reduce_adamw_cast_bytes_per_launch")
+            rec = json.load(f)
+        if rec.get("kernel_source_sha256") == kernel_source_sha256():
+            traffic = rec.get("grad_reduce_adamw_cast_bytes_per_launch")
+            traffic_note = rec.get("source", "")
+        else:
+            traffic_note = "the kernel changed since the ncu capture: traffic withheld"
+
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
@@ -496,7 +531,7 @@ def run_ours(args):
         "hbm_gbs": step_bytes / (ms_step * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "kernel": "grad_reduce_adamw_cast",
                      "achieved": ach_upd, "peak": peak, "unit": "GB/s", "frac": ach_upd / peak,
-                     "traffic": traffic, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": traffic, "traffic_note": traffic_note, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                      "bytes_per_launch": bytes_upd, "avg_launch_ms": upd_avg,
                      "bytes_per_param": 26 + 2 * R},
         "prepass": ({"kernel": "grad_sqnorm", "achieved": ach_pre, "unit": "GB/s", "frac": ach_pre / peak,

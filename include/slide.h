@@ -88,7 +88,11 @@ enum {
 };
 
 enum {
-    SLIDE_FLAG_CHECK_FINITE = 1u      /* check the mean gradient for NaN/Inf each step */
+    SLIDE_FLAG_CHECK_FINITE = 1u,       /* check the mean gradient for NaN/Inf each step */
+    SLIDE_FLAG_TEST_PIPELINE_STALL = 2u /* tests only: the update kernel's copy producer issues nothing,
+                                           so the consumers' bounded wait (2 s) runs out and the step
+                                           reports SLIDE_ERR_TIMEOUT through slide_layer_status; the
+                                           layer's values are then undefined */
 };
 
 /* Adam hyper-parameters (FP32).  Valid: lr >= 0, 0 <= beta1 < 1,

@@ -34,6 +34,7 @@ STATUS_NAMES = {0: "SLIDE_OK", 1: "SLIDE_ERR_INVALID_ARG", 2: "SLIDE_ERR_OOM_DEV
 SLIDE_RESIDENCY_HBM = 0
 SLIDE_RESIDENCY_HOST_STREAMED = 1
 SLIDE_FLAG_CHECK_FINITE = 1
+SLIDE_FLAG_TEST_PIPELINE_STALL = 2
 SLIDE_MAX_REPLICAS = 8
 
 
@@ -249,9 +250,10 @@ def slide_layer_last_clip_coef(st: SlideState, layer: int) -> float:
 
 
 def slide_layer_status(st: SlideState, layer: int) -> int:
-    """Returns the status code (SLIDE_OK or SLIDE_ERR_NONFINITE); raises on other errors."""
+    """Returns the status code (SLIDE_OK, SLIDE_ERR_NONFINITE or
+    SLIDE_ERR_TIMEOUT); raises on other errors."""
     rc = _lib().slide_layer_status(C.c_void_p(st.handle), layer)
-    if rc not in (SLIDE_OK, SLIDE_ERR_NONFINITE):
+    if rc not in (SLIDE_OK, SLIDE_ERR_NONFINITE, SLIDE_ERR_TIMEOUT):
         _check(rc)
     return rc
 

@@ -56,6 +56,7 @@ constexpr int kStages = 2;               // shared-memory ring depth
 constexpr int kConsumerWarps = 8;        // kTile = 256 consumer threads x 8 parameters
 constexpr int kPipeThreads = (kConsumerWarps + 1) * 32;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr uint32_t kWaitLimitTries = 1u << 26;
 static_assert(kTile == kConsumerWarps * 32 * 8, "each consumer thread owns 8 parameters of a tile");
 
 constexpr unsigned kStatusNonFinite = 1u;
@@ -74,6 +75,7 @@ struct KArgs {
     float max_norm;
     float *coef_out;
     unsigned *status;
+    int test_stall;  // test only: the producer issues nothing, so the consumers' bounded wait runs out
 };
 
 __device__ __forceinline__ float bf16_lo(uint32_t word) { return __uint_as_float(word << 16); }
@@ -229,19 +231,21 @@ __device__ __forceinline__ unsigned long long global_ns()
 }
 
 // Wait until the phase of `bar` with the given parity has completed; false if
-// kWaitLimitNs of wall time passed first.
+// kWaitLimitNs of wall time (or, as a second bound, kWaitLimitTries polls)
+// passed first.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
 {
     if (mbar_try_wait(bar, parity))
         return true;
     const unsigned long long t0 = global_ns();
-    for (;;) {
+    for (uint32_t round = 0; round < kWaitLimitTries / 64; ++round) {
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity))
                 return true;
         if (global_ns() - t0 > kWaitLimitNs)
             return false;
     }
+    return false;
 }
 
 // 1-D bulk copy global -> shared, completing `bytes` on the mbarrier.
@@ -290,7 +294,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_grad_reduce_adamw_cast(KArg
 
     if (warp == kConsumerWarps) {
         // ---- producer: one thread issues the bulk copies of each tile ----
-        if (lane != 0)
+        if (lane != 0 || a.test_stall)
             return;
         int stage = 0;
         uint32_t phase = 0;
@@ -662,7 +666,7 @@ cudaError_t launch_grad_sqnorm(const ReplicaPtrs &g, int R, int64_t n, const Cli
 cudaError_t launch_grad_reduce_adamw_cast(const ReplicaPtrs &g, int R, int64_t n, float *theta,
                                           float *m, float *v, uint16_t *w, const AdamScalars &s,
                                           const ClipScratch *clip, int n_partials, float max_norm,
-                                          bool check_finite, int device, cudaStream_t stream)
+                                          bool check_finite, int device, cudaStream_t stream, bool test_stall)
 {
     const bool do_clip = clip != nullptr && clip->partials != nullptr && max_norm > 0.0f;
     KArgs a{};
@@ -678,6 +682,7 @@ cudaError_t launch_grad_reduce_adamw_cast(const ReplicaPtrs &g, int R, int64_t n
     a.max_norm = max_norm;
     a.coef_out = do_clip ? clip->coef : nullptr;
     a.status = clip ? clip->status : nullptr;
+    a.test_stall = test_stall ? 1 : 0;
     switch (R) {
     case 1: return launch_step_flags<1>(a, do_clip, check_finite, device, stream);
     case 2: return launch_step_flags<2>(a, do_clip, check_finite, device, stream);

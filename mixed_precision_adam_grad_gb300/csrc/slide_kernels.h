@@ -43,7 +43,8 @@ cudaError_t launch_grad_sqnorm(const ReplicaPtrs &g, int R, int64_t n, const Cli
 cudaError_t launch_grad_reduce_adamw_cast(const ReplicaPtrs &g, int R, int64_t n, float *theta,
                                           float *m, float *v, uint16_t *w, const AdamScalars &s,
                                           const ClipScratch *clip, int n_partials, float max_norm,
-                                          bool check_finite, int device, cudaStream_t stream);
+                                          bool check_finite, int device, cudaStream_t stream,
+                                          bool test_stall = false);
 
 // w[i] = bf16_rne(src[i]) (used when a caller overwrites a master copy).
 cudaError_t launch_cast_bf16(const float *src, uint16_t *w, int64_t n, cudaStream_t stream);

@@ -32,12 +32,12 @@
 //  reverse sweep, l = L-1 .. 0, slot s = l%2:
 //    H2D stream:     master/m/v of l -> slot s, chunk by chunk; chunk k of each
 //                    array first waits for the D2H of the same chunk of the
-//                    unit that last used slot s (l+2, or l+1's neighbour in
-//                    processing order), so the copy-in of l trails the
-//                    copy-out of l+2 by one chunk;
-//    compute stream: wait for the H2D of l and for the D2H of the BF16 copy of
-//                    l+2; grad_fn(l) fills the R replicas; clip pre-pass and
-//                    the fused kernel update slot s in place;
+//                    unit that last used slot s (l+2), so the copy-in of l
+//                    trails the copy-out of l+2 by one chunk;
+//    compute stream: once the master of l has landed, grad_fn(l) fills the R
+//                    replicas (while m and v still arrive); then, after the
+//                    rest of l's H2D and the D2H of the BF16 copy of l+2, the
+//                    clip pre-pass and the fused kernel update slot s in place;
 //    D2H stream:     wait for the kernel; BF16 copy, then master/m/v of l back
 //                    to the host, chunk by chunk, each chunk recording the
 //                    event the next copy-in to the same bytes waits for.
@@ -84,8 +84,9 @@ struct StreamEngine {
     int64_t chunk_bytes = 0;
     int chunks_per_region = 0;
     cudaStream_t s_h2d = nullptr, s_comp = nullptr, s_d2h = nullptr;
-    std::vector<cudaEvent_t> h2d_done;  // per unit
-    std::vector<cudaEvent_t> kern_done; // per unit
+    std::vector<cudaEvent_t> theta_done;  // per unit: the master has landed in its slot
+    std::vector<cudaEvent_t> h2d_done;    // per unit: master, m and v have landed
+    std::vector<cudaEvent_t> kern_done;   // per unit
     cudaEvent_t fwd_done = nullptr;
     cudaEvent_t sweep_done[3] = {nullptr, nullptr, nullptr};  // end of the H2D, compute, D2H streams
 };
@@ -106,6 +107,9 @@ static void destroy_engine_objects(StreamEngine *E)
             cudaEventDestroy(s.w_freed);
     }
     for (cudaEvent_t ev : E->h2d_done)
+        if (ev)
+            cudaEventDestroy(ev);
+    for (cudaEvent_t ev : E->theta_done)
         if (ev)
             cudaEventDestroy(ev);
     for (cudaEvent_t ev : E->kern_done)
@@ -172,9 +176,12 @@ slide_status engine_create(slide_state *st)
     }
     const size_t L = st->layers.size();
     E->h2d_done.assign(L, nullptr);
+    E->theta_done.assign(L, nullptr);
     E->kern_done.assign(L, nullptr);
     for (size_t l = 0; l < L && e == cudaSuccess; ++l) {
         e = cudaEventCreateWithFlags(&E->h2d_done[l], cudaEventDisableTiming);
+        if (e == cudaSuccess)
+            e = cudaEventCreateWithFlags(&E->theta_done[l], cudaEventDisableTiming);
         if (e == cudaSuccess)
             e = cudaEventCreateWithFlags(&E->kern_done[l], cudaEventDisableTiming);
     }
@@ -291,8 +298,11 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
         const LayerState &U = st->layers[l];
         const float *src[kRegions] = {U.theta, U.m, U.v};
         cudaError_t err = cudaSuccess;
-        for (int r = 0; r < kRegions && err == cudaSuccess; ++r)
+        for (int r = 0; r < kRegions && err == cudaSuccess; ++r) {
             err = copy_region(E, s, r, s.arr[r], src[r], (size_t)U.n * 4, cudaMemcpyHostToDevice, E->s_h2d);
+            if (r == 0 && err == cudaSuccess)
+                err = cudaEventRecord(E->theta_done[l], E->s_h2d);
+        }
         if (err == cudaSuccess)
             err = cudaEventRecord(E->h2d_done[l], E->s_h2d);
         return err;
@@ -310,10 +320,10 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
             if (e != cudaSuccess)
                 break;
         }
-        // update l on the compute stream
-        e = cudaStreamWaitEvent(E->s_comp, E->h2d_done[l], 0);
-        if (e == cudaSuccess)
-            e = cudaStreamWaitEvent(E->s_comp, s.w_freed, 0);
+        // gradients of l on the compute stream as soon as its master has landed
+        // (m and v keep arriving meanwhile), then the update once all of the
+        // unit is in and the slot's BF16 buffer has been written back
+        e = cudaStreamWaitEvent(E->s_comp, E->theta_done[l], 0);
         if (e != cudaSuccess)
             break;
         if (U.n > 0) {
@@ -327,6 +337,13 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
                                                  std::to_string(l));
                 break;
             }
+        }
+        e = cudaStreamWaitEvent(E->s_comp, E->h2d_done[l], 0);
+        if (e == cudaSuccess)
+            e = cudaStreamWaitEvent(E->s_comp, s.w_freed, 0);
+        if (e != cudaSuccess)
+            break;
+        if (U.n > 0) {
             ReplicaPtrs g{};
             for (int r = 0; r < R; ++r)
                 g.p[r] = s.g[r];

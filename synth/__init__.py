@@ -42,6 +42,12 @@ class ModelGrads(C.Structure):
                 ("seg_scale", C.c_void_p), ("default_scale", C.c_float)]
 
 
+class PoolGrads(C.Structure):
+    """User data of the pool-copy gradient callback."""
+    _fields_ = [("n_replicas", C.c_int32), ("n_pool", C.c_int32), ("step", C.c_uint32),
+                ("pad_", C.c_int32), ("unit_numel", C.c_void_p), ("pool", C.c_void_p)]
+
+
 def _stale(so, srcs):
     return not os.path.exists(so) or any(os.path.getmtime(so) < os.path.getmtime(s) for s in srcs)
 
@@ -102,6 +108,7 @@ def dev():
         L.syn_dev_fill_grad.argtypes = [P, i64, i64, C.POINTER(GradSpec), u32, u32, u32, C.c_float, P]
         L.syn_dev_normals.argtypes = [P, i64, u32, u32, u32, u32, u32, P]
         L.syn_dev_grad_fn.argtypes = [P, C.c_int32, P, P]
+        L.syn_dev_pool_grad_fn.argtypes = [P, C.c_int32, P, P]
         _dev = L
     return _dev
 
@@ -109,6 +116,11 @@ def dev():
 def grad_fn_address() -> int:
     """Address of the C gradient callback (for the streamed model step)."""
     return C.cast(dev().syn_dev_grad_fn, C.c_void_p).value
+
+
+def pool_grad_fn_address() -> int:
+    """Address of the pool-copy gradient callback."""
+    return C.cast(dev().syn_dev_pool_grad_fn, C.c_void_p).value
 
 
 def spec(seed, kind=GRAD_NORMAL, zero_prob=0.0) -> GradSpec:

@@ -110,4 +110,30 @@ int syn_dev_grad_fn(void *user, int32_t layer, void *const *replicas, cudaStream
     return 0;
 }
 
+/* Gradient callback that copies pre-generated replicas from a device pool
+ * (benchmarking the streamed step without timing the generator): unit l at
+ * step t gets pool entry (l + t) % n_pool, replicas r = 0..R-1. */
+typedef struct {
+    int32_t n_replicas;
+    int32_t n_pool;
+    uint32_t step;
+    int32_t pad_;
+    const int64_t *unit_numel;   /* host array [n_units] */
+    void *const *pool;           /* host array [n_pool * n_replicas] of device pointers */
+} syn_pool_grads;
+
+int syn_dev_pool_grad_fn(void *user, int32_t layer, void *const *replicas, cudaStream_t s)
+{
+    const syn_pool_grads *p = (const syn_pool_grads *)user;
+    if (!p || layer < 0 || p->n_pool < 1) return -1;
+    const int k = (int)(((uint32_t)layer + p->step) % (uint32_t)p->n_pool);
+    const size_t bytes = (size_t)p->unit_numel[layer] * 2;
+    for (int32_t r = 0; r < p->n_replicas; ++r) {
+        cudaError_t e = cudaMemcpyAsync(replicas[r], p->pool[k * p->n_replicas + r], bytes,
+                                        cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return (int)e;
+    }
+    return 0;
+}
+
 }  // extern "C"

@@ -125,6 +125,36 @@ def test_small_parity_clip(S, R, clip):
             assert r["not_bit_equal"] == 0, r
 
 
+@pytest.mark.parametrize("scale", [1e-8, 1e-10, 1e-30])
+def test_eps_regime_bit_exact(S, scale):
+    """Gradients around and far below eps (1e-8): the update is governed by
+    the eps term; still the same FP32 operations on both sides."""
+    n, R = 70001, 4
+    w = W.Workload("eps", [W.Unit("l", [("flat", n)])], R=R, steps=4, seed=41, grad_scale=scale, lr=1e-3)
+    hp_dev = S.hparams(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, 0.0)
+    hp_or = pu.hp_oracle(w)
+    th = synth.master(n, w.seed)
+    m, v, wb = np.zeros(n, np.float32), np.zeros(n, np.float32), np.zeros(n, np.uint16)
+    st = S.slide_state_create([n], R)
+    try:
+        S.slide_layer_set(st, 0, master=th, step=0)
+        grads = [dev_u16(n) for _ in range(R)]
+        for t in range(1, 5):
+            for r in range(R):
+                pu.unit_grad_dev(w, 0, t, r, grads[r].data_ptr())
+            S.slide_layer_step(st, 0, grads, hp_dev)
+            oracle.layer_step([pu.unit_grad_host(w, 0, t, r) for r in range(R)], th, m, v, wb, hp_or, t)
+        a, b, c = (np.empty(n, np.float32) for _ in range(3))
+        gw = np.empty(n, np.uint16)
+        S.slide_layer_get(st, 0, a, b, c, gw)
+        rep = [pu.compare_fp32("theta", a, th), pu.compare_fp32("m", b, m), pu.compare_fp32("v", c, v),
+               pu.compare_bf16("w", gw, wb)]
+        pu.assert_parity(rep)
+        assert all(r["not_bit_equal"] == 0 for r in rep), rep
+    finally:
+        S.slide_state_destroy(st)
+
+
 def test_external_bf16_out_and_empty_layer(S):
     run_small(S, [0, 5, 4099], 2, clip=0.5, bf16_external=True)
 
