@@ -285,6 +285,34 @@ def link_probe(torch, nbytes=1 << 30, reps=20):
     return out
 
 
+def _union(intervals):
+    out = []
+    for a, b in sorted(intervals):
+        if out and a <= out[-1][1]:
+            out[-1][1] = max(out[-1][1], b)
+        else:
+            out.append([a, b])
+    return out
+
+
+def timeline_overlap(units, fwd_end):
+    """Busy time of the host->device and device->host copies in the last
+    streamed step (from the engine's per-unit events) and how much of it ran
+    at the same time."""
+    import math
+    h2d = _union([(0.0, fwd_end)] + [(u["h2d_begin"], u["h2d_end"]) for u in units
+                                     if not math.isnan(u["h2d_begin"])])
+    d2h = _union([(u["d2h_begin"], u["d2h_end"]) for u in units if not math.isnan(u["d2h_begin"])])
+    both = 0.0
+    for a, b in h2d:
+        for c, d in d2h:
+            both += max(0.0, min(b, d) - max(a, c))
+    end = max(iv[1] for iv in h2d + d2h)
+    return {"step_ms": end, "h2d_busy_ms": sum(b - a for a, b in h2d), "d2h_busy_ms": sum(b - a for a, b in d2h),
+            "both_busy_ms": both, "forward_sweep_ms": fwd_end,
+            "units_ms": [{k: round(v, 3) for k, v in u.items()} for u in units]}
+
+
 def run_streamed(args, S, torch, synth):
     """Host-resident streamed step of a whole model: s/step against the
     host-link roofline measured in the same run.  The gradient callback stands
@@ -331,6 +359,8 @@ def run_streamed(args, S, torch, synth):
             t0 = time.perf_counter()
             S.slide_model_step_streamed(st, fn_pool, pg, hp)      # returns after the last write-back
             times.append(time.perf_counter() - t0)
+        units_tl, fwd_end = S.slide_streamed_timeline(st)
+        overlap = timeline_overlap(units_tl, fwd_end)
         t0 = time.perf_counter()
         S.slide_model_step_streamed(st, fn_gen, mg, hp)
         gen_s = time.perf_counter() - t0
@@ -353,6 +383,7 @@ def run_streamed(args, S, torch, synth):
             "grad_callback": f"copies pre-generated replicas ({n_pool} sets, the workload's distribution) "
                              "from HBM into the window",
             "s_per_step_with_generator_callback": gen_s,
+            "timeline_last_step": overlap,
             "timing": "host wall clock around each synchronous model step"}
 
 
@@ -442,40 +473,69 @@ def run_ours(args):
         upd_ms = [e[1].elapsed_time(e[2]) for e in ev]
         ms_total = max_over_ranks(ms_total, dist)
 
-        # end to end through the public API: pinned host replicas in, BF16 copy out
+        # End to end through the public API: every step copies its R replicas
+        # from pinned host memory into the GPU and its BF16 copy back to pinned
+        # host memory.  Pipelined as a user would: two device replica buffers;
+        # the copy-in of step k+1 (copy stream) overlaps the update and the
+        # copy-out of step k (compute stream), ordered by events.
         e2e = None
         if not args.no_e2e:
             Ke = max(3, min(args.e2e_steps, K))
-            host_reps = [torch.empty(n, dtype=torch.int16, pin_memory=True) for _ in range(R)]
-            for r in range(R):
-                host_reps[r].copy_(batches[0][r][:n])
-            dev_reps = [torch.empty(n + 64, dtype=torch.int16, device="cuda") for _ in range(R)]
-            out_dev = torch.empty(n + 64, dtype=torch.int16, device="cuda")
-            out_host = torch.empty(n, dtype=torch.int16, pin_memory=True)
+            host_reps = [[torch.empty(n, dtype=torch.int16, pin_memory=True) for _ in range(R)] for _ in range(2)]
+            for b in range(2):
+                for r in range(R):
+                    host_reps[b][r].copy_(batches[b % len(batches)][r][:n])
+            dev_reps = [[torch.empty(n + 64, dtype=torch.int16, device="cuda") for _ in range(R)] for _ in range(2)]
+            out_dev = [torch.empty(n + 64, dtype=torch.int16, device="cuda") for _ in range(2)]
+            out_host = [torch.empty(n, dtype=torch.int16, pin_memory=True) for _ in range(2)]
+            copy_stream = torch.cuda.Stream()
+            landed = [torch.cuda.Event() for _ in range(2)]
+            consumed = [torch.cuda.Event() for _ in range(2)]
             torch.cuda.synchronize()
 
-            def e2e_step():
-                with torch.cuda.stream(stream):
+            def copy_in(k):
+                b = k % 2
+                copy_stream.wait_event(consumed[b])          # the step that read this buffer is done
+                with torch.cuda.stream(copy_stream):
                     for r in range(R):
-                        dev_reps[r][:n].copy_(host_reps[r], non_blocking=True)
-                    S.slide_layer_step(st, 0, dev_reps, hp, stream, out_dev)
-                    out_host.copy_(out_dev[:n], non_blocking=True)
+                        dev_reps[b][r][:n].copy_(host_reps[b][r], non_blocking=True)
+                    landed[b].record(copy_stream)
 
-            for _ in range(3):
-                e2e_step()
+            def step_out(k):
+                b = k % 2
+                stream.wait_event(landed[b])
+                S.slide_layer_step(st, 0, dev_reps[b], hp, stream, out_dev[b])
+                consumed[b].record(stream)
+                with torch.cuda.stream(stream):
+                    out_host[b].copy_(out_dev[b][:n], non_blocking=True)
+
+            def run_e2e(steps):
+                copy_in(0)
+                for k in range(steps):
+                    if k + 1 < steps:
+                        copy_in(k + 1)
+                    step_out(k)
+
+            for e in consumed:
+                e.record(stream)
+            run_e2e(3)
             torch.cuda.synchronize()
             if dist:
                 dist.barrier()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            for _ in range(Ke):
-                e2e_step()
+            copy_stream.wait_event(e0)
+            run_e2e(Ke)
+            copy_stream_done = torch.cuda.Event()
+            copy_stream_done.record(copy_stream)
+            stream.wait_event(copy_stream_done)
             e1.record(stream)
             torch.cuda.synchronize()
             ms_e2e = e0.elapsed_time(e1)
             ms_e2e = max_over_ranks(ms_e2e, dist)
             e2e = {"value": n * Ke * world / (ms_e2e * 1e-3) / 1e9, "unit": UNIT,
-                   "h2d_bytes_per_step": 2 * R * n, "d2h_bytes_per_step": 2 * n, "steps": Ke}
+                   "h2d_bytes_per_step": 2 * R * n, "d2h_bytes_per_step": 2 * n, "steps": Ke,
+                   "pipelining": "copy-in of step k+1 on a copy stream overlaps step k's update and copy-out"}
     finally:
         S.slide_state_destroy(st)
 

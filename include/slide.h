@@ -241,6 +241,16 @@ SLIDE_API slide_status slide_adamw_step_noalloc(int64_t n, int32_t n_replicas, c
                                                 const slide_adam_hparams *hp, int64_t step,
                                                 slide_stream_t stream);
 
+/* Timeline of the last slide_model_step_streamed, for tracing how the copies
+ * and the updates overlap (host-streamed residency).  out receives, for each
+ * unit l, 6 values in milliseconds from the start of that step:
+ *   [6l+0] copy-in of master/m/v began   [6l+1] master landed
+ *   [6l+2] copy-in ended                 [6l+3] update kernel ended
+ *   [6l+4] write-back began              [6l+5] write-back ended
+ * and out[6L] = end of the forward sweep (BF16 delivery); NaN where a unit
+ * did not get that far.  cap = number of doubles in out (>= 6L + 1). */
+SLIDE_API slide_status slide_streamed_timeline(slide_state *st, double *out, int64_t cap);
+
 /* Message of the last error on this host thread ("" if none). */
 SLIDE_API const char *slide_last_error(void);
 

@@ -86,6 +86,8 @@ def _load():
     L.slide_layer_last_clip_coef.restype = S
     L.slide_layer_status.argtypes = [P, C.c_int32]
     L.slide_layer_status.restype = S
+    L.slide_streamed_timeline.argtypes = [P, C.POINTER(C.c_double), C.c_int64]
+    L.slide_streamed_timeline.restype = S
     L.slide_trace_events.argtypes = [P, P, P, P]
     L.slide_trace_events.restype = S
     L.slide_adamw_step_noalloc.argtypes = [C.c_int64, C.c_int32, C.POINTER(C.c_void_p), P, P, P, P,
@@ -279,3 +281,14 @@ def slide_adamw_step_noalloc(n: int, grad_replicas, master, m, v, bf16_out, hp: 
     arr = (C.c_void_p * max(1, len(ptrs)))(*ptrs)
     _check(_lib().slide_adamw_step_noalloc(n, len(ptrs), arr, _ptr(master), _ptr(m), _ptr(v), _ptr(bf16_out),
                                            C.byref(hp), step, _stream(stream)))
+
+
+def slide_streamed_timeline(st: SlideState):
+    """Per-unit timeline (ms) of the last streamed step: a list of dicts and
+    the end of the forward sweep."""
+    L = len(st.layer_numel)
+    buf = (C.c_double * (6 * L + 1))()
+    _check(_lib().slide_streamed_timeline(C.c_void_p(st.handle), buf, 6 * L + 1))
+    keys = ("h2d_begin", "master_landed", "h2d_end", "update_end", "d2h_begin", "d2h_end")
+    units = [dict(zip(keys, buf[6 * l:6 * l + 6])) for l in range(L)]
+    return units, buf[6 * L]

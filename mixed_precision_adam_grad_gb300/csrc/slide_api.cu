@@ -515,6 +515,19 @@ slide_status slide_trace_events(slide_state *st, void *ev_prepass_start, void *e
     return SLIDE_OK;
 }
 
+slide_status slide_streamed_timeline(slide_state *st, double *out, int64_t cap)
+{
+    if (!st || !out)
+        return fail(SLIDE_ERR_INVALID_ARG, "state or out is NULL");
+    if (st->cfg.residency != SLIDE_RESIDENCY_HOST_STREAMED || !st->engine)
+        return fail(SLIDE_ERR_STATE, "the timeline belongs to the host-streamed residency");
+    DeviceGuard guard(st->device);
+    slide_status rc = engine_timeline(st, out, cap);
+    if (rc == SLIDE_OK)
+        clear_error();
+    return rc;
+}
+
 slide_status slide_model_step_streamed(slide_state *st, slide_grad_fn fn, void *user,
                                        const slide_adam_hparams *hp)
 {

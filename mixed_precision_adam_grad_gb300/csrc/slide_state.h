@@ -77,5 +77,6 @@ slide_status engine_create(slide_state *st);
 void engine_destroy(slide_state *st);
 size_t engine_device_bytes(const slide_config &cfg, int64_t max_numel);
 slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const slide_adam_hparams &hp);
+slide_status engine_timeline(slide_state *st, double *out, int64_t cap);
 
 }  // namespace slide

@@ -89,6 +89,11 @@ struct StreamEngine {
     std::vector<cudaEvent_t> kern_done;   // per unit
     cudaEvent_t fwd_done = nullptr;
     cudaEvent_t sweep_done[3] = {nullptr, nullptr, nullptr};  // end of the H2D, compute, D2H streams
+    // timeline of the last step (timing events): start, and per unit the
+    // begin of its copy-in and the begin/end of its write-back
+    cudaEvent_t step_start = nullptr;
+    std::vector<cudaEvent_t> h2d_begin, d2h_begin, d2h_end;
+    std::vector<char> recorded;  // unit reached write-back in the last step
 };
 
 size_t engine_device_bytes(const slide_config &cfg, int64_t max_numel)
@@ -117,6 +122,12 @@ static void destroy_engine_objects(StreamEngine *E)
             cudaEventDestroy(ev);
     if (E->fwd_done)
         cudaEventDestroy(E->fwd_done);
+    if (E->step_start)
+        cudaEventDestroy(E->step_start);
+    for (auto *vec : {&E->h2d_begin, &E->d2h_begin, &E->d2h_end})
+        for (cudaEvent_t ev : *vec)
+            if (ev)
+                cudaEventDestroy(ev);
     for (cudaEvent_t ev : E->sweep_done)
         if (ev)
             cudaEventDestroy(ev);
@@ -178,15 +189,28 @@ slide_status engine_create(slide_state *st)
     E->h2d_done.assign(L, nullptr);
     E->theta_done.assign(L, nullptr);
     E->kern_done.assign(L, nullptr);
+    E->h2d_begin.assign(L, nullptr);
+    E->d2h_begin.assign(L, nullptr);
+    E->d2h_end.assign(L, nullptr);
+    E->recorded.assign(L, 0);
+    // the events of the timeline keep timing; the others are sync-only
     for (size_t l = 0; l < L && e == cudaSuccess; ++l) {
-        e = cudaEventCreateWithFlags(&E->h2d_done[l], cudaEventDisableTiming);
+        e = cudaEventCreate(&E->h2d_done[l]);
         if (e == cudaSuccess)
-            e = cudaEventCreateWithFlags(&E->theta_done[l], cudaEventDisableTiming);
+            e = cudaEventCreate(&E->theta_done[l]);
         if (e == cudaSuccess)
-            e = cudaEventCreateWithFlags(&E->kern_done[l], cudaEventDisableTiming);
+            e = cudaEventCreate(&E->kern_done[l]);
+        if (e == cudaSuccess)
+            e = cudaEventCreate(&E->h2d_begin[l]);
+        if (e == cudaSuccess)
+            e = cudaEventCreate(&E->d2h_begin[l]);
+        if (e == cudaSuccess)
+            e = cudaEventCreate(&E->d2h_end[l]);
     }
     if (e == cudaSuccess)
-        e = cudaEventCreateWithFlags(&E->fwd_done, cudaEventDisableTiming);
+        e = cudaEventCreate(&E->fwd_done);
+    if (e == cudaSuccess)
+        e = cudaEventCreate(&E->step_start);
     for (int k = 0; k < 3 && e == cudaSuccess; ++k)
         e = cudaEventCreateWithFlags(&E->sweep_done[k], cudaEventDisableTiming);
     if (e == cudaSuccess)
@@ -280,6 +304,9 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
     slide_status rc = SLIDE_OK;
     int done_units = 0;  // units whose update and write-back were enqueued (from L-1 down)
 
+    for (int l = 0; l < L; ++l)
+        E->recorded[l] = 0;
+    e = cudaEventRecord(E->step_start, E->s_h2d);
     // forward sweep: deliver the BF16 copy of every unit, in order
     for (int l = 0; l < L && e == cudaSuccess; ++l) {
         Slot &s = E->slots[l % kSlots];
@@ -297,7 +324,7 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
         Slot &s = E->slots[l % kSlots];
         const LayerState &U = st->layers[l];
         const float *src[kRegions] = {U.theta, U.m, U.v};
-        cudaError_t err = cudaSuccess;
+        cudaError_t err = cudaEventRecord(E->h2d_begin[l], E->s_h2d);
         for (int r = 0; r < kRegions && err == cudaSuccess; ++r) {
             err = copy_region(E, s, r, s.arr[r], src[r], (size_t)U.n * 4, cudaMemcpyHostToDevice, E->s_h2d);
             if (r == 0 && err == cudaSuccess)
@@ -364,6 +391,8 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
             break;
         // write l back: the BF16 copy first (frees the slot for the next kernel), then master/m/v
         e = cudaStreamWaitEvent(E->s_d2h, E->kern_done[l], 0);
+        if (e == cudaSuccess)
+            e = cudaEventRecord(E->d2h_begin[l], E->s_d2h);
         if (e == cudaSuccess && U.n > 0)
             e = cudaMemcpyAsync(U.w, s.w, (size_t)U.n * 2, cudaMemcpyDeviceToHost, E->s_d2h);
         if (e == cudaSuccess)
@@ -372,7 +401,11 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
         for (int r = 0; r < kRegions && e == cudaSuccess; ++r)
             e = copy_region(E, s, r, dst[r], s.arr[r], (size_t)U.n * 4, cudaMemcpyDeviceToHost, E->s_d2h);
         if (e == cudaSuccess)
+            e = cudaEventRecord(E->d2h_end[l], E->s_d2h);
+        if (e == cudaSuccess) {
+            E->recorded[l] = 1;
             ++done_units;
+        }
     }
     if (e != cudaSuccess && rc == SLIDE_OK)
         rc = fail_cuda(e, "streamed step: enqueue");
@@ -415,6 +448,40 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
     }
     st->aborted = true;
     return rc;
+}
+
+// Timeline of the last step: per unit, milliseconds from the step's start to
+// [copy-in begin, master landed, copy-in end, update end, write-back begin,
+// write-back end]; then the end of the forward sweep.  NaN where a unit did
+// not get that far.
+slide_status engine_timeline(slide_state *st, double *out, int64_t cap)
+{
+    StreamEngine *E = st->engine;
+    const int L = (int)st->layers.size();
+    if (cap < 6 * (int64_t)L + 1)
+        return fail(SLIDE_ERR_INVALID_ARG, "timeline buffer needs 6 * n_layers + 1 doubles");
+    const double nan = __builtin_nan("");
+    auto since = [&](cudaEvent_t ev) -> double {
+        float ms = 0.0f;
+        return cudaEventElapsedTime(&ms, E->step_start, ev) == cudaSuccess ? (double)ms : nan;
+    };
+    for (int l = 0; l < L; ++l) {
+        double *o = out + 6 * l;
+        if (!E->recorded[l]) {
+            for (int k = 0; k < 6; ++k)
+                o[k] = nan;
+            continue;
+        }
+        o[0] = since(E->h2d_begin[l]);
+        o[1] = since(E->theta_done[l]);
+        o[2] = since(E->h2d_done[l]);
+        o[3] = since(E->kern_done[l]);
+        o[4] = since(E->d2h_begin[l]);
+        o[5] = since(E->d2h_end[l]);
+    }
+    out[6 * L] = since(E->fwd_done);
+    cudaGetLastError();  // a NaN entry leaves a sticky-free "not ready" error behind
+    return SLIDE_OK;
 }
 
 }  // namespace slide

@@ -75,6 +75,13 @@ def lib():
         L.oracle_bf16_to_f32_array.argtypes = [C.c_int64, P, P]
         L.oracle_step_scalars_for.argtypes = [C.POINTER(Hparams), C.c_int64, C.POINTER(StepScalars)]
         L.oracle_grad_mean.argtypes = [C.c_int64, C.c_int32, P, P]
+        L.oracle_grad_mean_f32.argtypes = [C.c_int64, C.c_int32, P, P]
+        L.oracle_layer_step_f32g.restype = C.c_float
+        L.oracle_layer_step_f32g.argtypes = [C.c_int64, C.c_int32, P, P, P, P, P,
+                                             C.POINTER(Hparams), C.c_int64]
+        L.oracle_layer_step_f64_f32g.restype = C.c_double
+        L.oracle_layer_step_f64_f32g.argtypes = [C.c_int64, C.c_int32, P, P, P, P,
+                                                 C.POINTER(Hparams), C.c_int64]
         L.oracle_grad_sqnorm.restype = C.c_double
         L.oracle_grad_sqnorm.argtypes = [C.c_int64, P]
         L.oracle_clip_coef.restype = C.c_float
@@ -107,9 +114,13 @@ def _ptr(a) -> int:
 
 
 def _replica_table(grads):
+    """Pointer table of the replicas (all BF16 bit patterns as uint16, or all FP32)."""
     n = None
+    dtype = grads[0].dtype if len(grads) else np.uint16
+    if dtype not in (np.uint16, np.float32):
+        raise TypeError("replicas must be uint16 (BF16 bits) or float32")
     for g in grads:
-        _as(g, np.uint16)
+        _as(g, dtype)
         if n is None:
             n = g.size
         elif g.size != n:
@@ -138,10 +149,15 @@ def step_scalars(hp: Hparams, t: int) -> StepScalars:
     return s
 
 
+def _is_f32(grads):
+    return len(grads) > 0 and grads[0].dtype == np.float32
+
+
 def grad_mean(grads) -> np.ndarray:
     tab, n = _replica_table(grads)
     gm = np.empty(n, np.float32)
-    lib().oracle_grad_mean(n, len(grads), tab, _ptr(gm))
+    fn = lib().oracle_grad_mean_f32 if _is_f32(grads) else lib().oracle_grad_mean
+    fn(n, len(grads), tab, _ptr(gm))
     return gm
 
 
@@ -183,8 +199,8 @@ def layer_step(grads, theta, m, v, w, hp: Hparams, t: int) -> float:
         if w.size != n:
             raise ValueError("length mismatch")
         wp = _ptr(w)
-    c = lib().oracle_layer_step(n, len(grads), tab, _ptr(theta), _ptr(m), _ptr(v),
-                                wp, C.byref(hp), t)
+    fn = lib().oracle_layer_step_f32g if _is_f32(grads) else lib().oracle_layer_step
+    c = fn(n, len(grads), tab, _ptr(theta), _ptr(m), _ptr(v), wp, C.byref(hp), t)
     if c < 0:
         raise MemoryError("oracle_layer_step: allocation failed")
     return c
@@ -196,8 +212,8 @@ def layer_step_f64(grads, theta, m, v, hp: Hparams, t: int) -> float:
         _as(a, np.float64)
         if a.size != n:
             raise ValueError("length mismatch")
-    c = lib().oracle_layer_step_f64(n, len(grads), tab, _ptr(theta), _ptr(m), _ptr(v),
-                                    C.byref(hp), t)
+    fn = lib().oracle_layer_step_f64_f32g if _is_f32(grads) else lib().oracle_layer_step_f64
+    c = fn(n, len(grads), tab, _ptr(theta), _ptr(m), _ptr(v), C.byref(hp), t)
     if c < 0:
         raise MemoryError("oracle_layer_step_f64: allocation failed")
     return c

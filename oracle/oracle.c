@@ -95,6 +95,17 @@ void oracle_grad_mean(int64_t n, int32_t R, const uint16_t *const *g, float *gm)
     }
 }
 
+void oracle_grad_mean_f32(int64_t n, int32_t R, const float *const *g, float *gm)
+{
+    float fr = (float)R;
+    for (int64_t i = 0; i < n; ++i) {
+        float s = g[0][i];
+        for (int32_t r = 1; r < R; ++r)
+            s = s + g[r][i];
+        gm[i] = s / fr;
+    }
+}
+
 /* ---- a2: optional global clip of the layer's mean gradient ---------------
  * Not on the pages; the benchmark workload asks for a global grad-norm clip.
  * The norm is the L2 norm of the whole layer's mean gradient (all of its
@@ -184,22 +195,30 @@ float oracle_layer_step(int64_t n, int32_t R, const uint16_t *const *g,
     return coef;
 }
 
+float oracle_layer_step_f32g(int64_t n, int32_t R, const float *const *g,
+                             float *theta, float *m, float *v, uint16_t *w,
+                             const oracle_hparams *hp, int64_t t)
+{
+    float *gm = (float *)malloc((size_t)(n > 0 ? n : 1) * sizeof(float));
+    if (!gm)
+        return -1.0f;
+    oracle_grad_mean_f32(n, R, g, gm);
+    float coef = 1.0f;
+    if (hp->max_grad_norm > 0.0f)
+        coef = oracle_clip_coef(oracle_grad_sqnorm(n, gm), hp->max_grad_norm);
+    oracle_adamw_update(n, gm, coef, theta, m, v, w, hp, t);
+    free(gm);
+    return coef;
+}
+
 /* ---- float64 brute force --------------------------------------------------
  * The same step with every quantity in double and the textbook arrangement
  * of the bias correction (corrected moments m_hat, v_hat formed explicitly). */
-double oracle_layer_step_f64(int64_t n, int32_t R, const uint16_t *const *g,
-                             double *theta, double *m, double *v,
-                             const oracle_hparams *hp, int64_t t)
+/* The double-precision update given the double mean gradient gm (clipped in
+ * place when max_grad_norm > 0); returns the clip coefficient. */
+static double f64_update(int64_t n, double *gm, double *theta, double *m, double *v,
+                         const oracle_hparams *hp, int64_t t)
 {
-    double *gm = (double *)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
-    if (!gm)
-        return -1.0;
-    for (int64_t i = 0; i < n; ++i) {
-        double s = 0.0;
-        for (int32_t r = 0; r < R; ++r)
-            s += (double)oracle_bf16_to_f32(g[r][i]);
-        gm[i] = s / (double)R;
-    }
     double coef = 1.0;
     if (hp->max_grad_norm > 0.0f) {
         double sq = 0.0;
@@ -219,6 +238,41 @@ double oracle_layer_step_f64(int64_t n, int32_t R, const uint16_t *const *g,
         double vhat = v[i] / bc2;
         theta[i] = theta[i] * (1.0 - lr * wd) - lr * mhat / (sqrt(vhat) + eps);
     }
+    return coef;
+}
+
+double oracle_layer_step_f64(int64_t n, int32_t R, const uint16_t *const *g,
+                             double *theta, double *m, double *v,
+                             const oracle_hparams *hp, int64_t t)
+{
+    double *gm = (double *)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+    if (!gm)
+        return -1.0;
+    for (int64_t i = 0; i < n; ++i) {
+        double s = 0.0;
+        for (int32_t r = 0; r < R; ++r)
+            s += (double)oracle_bf16_to_f32(g[r][i]);
+        gm[i] = s / (double)R;
+    }
+    double coef = f64_update(n, gm, theta, m, v, hp, t);
+    free(gm);
+    return coef;
+}
+
+double oracle_layer_step_f64_f32g(int64_t n, int32_t R, const float *const *g,
+                                  double *theta, double *m, double *v,
+                                  const oracle_hparams *hp, int64_t t)
+{
+    double *gm = (double *)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+    if (!gm)
+        return -1.0;
+    for (int64_t i = 0; i < n; ++i) {
+        double s = 0.0;
+        for (int32_t r = 0; r < R; ++r)
+            s += (double)g[r][i];
+        gm[i] = s / (double)R;
+    }
+    double coef = f64_update(n, gm, theta, m, v, hp, t);
     free(gm);
     return coef;
 }

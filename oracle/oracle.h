@@ -75,6 +75,12 @@ void oracle_step_scalars_for(const oracle_hparams *hp, int64_t t, oracle_step_sc
 /* a1: gm[i] = (sum_r g[r][i], summed in FP32 in replica order) / R */
 void oracle_grad_mean(int64_t n, int32_t R, const uint16_t *const *g, float *gm);
 
+/* a1 with FP32 gradient replicas (FP32 gradient accumulation, "Accelerating
+ * the Training of Large Language Models ...", section 3 and the experimental
+ * setup: BF16 training with FP32 gradients): the same rule, FP32 sum in
+ * replica order, divided by R. */
+void oracle_grad_mean_f32(int64_t n, int32_t R, const float *const *g, float *gm);
+
 /* a2: sum of gm[i]^2 in double, index order; coef = min(1, c/(sqrt(s)+1e-6)) */
 double oracle_grad_sqnorm(int64_t n, const float *gm);
 float  oracle_clip_coef(double sqnorm, float max_norm);
@@ -92,6 +98,11 @@ float oracle_layer_step(int64_t n, int32_t R, const uint16_t *const *g,
                         float *theta, float *m, float *v, uint16_t *w,
                         const oracle_hparams *hp, int64_t t);
 
+/* One whole layer step with FP32 gradient replicas (see oracle_grad_mean_f32). */
+float oracle_layer_step_f32g(int64_t n, int32_t R, const float *const *g,
+                             float *theta, float *m, float *v, uint16_t *w,
+                             const oracle_hparams *hp, int64_t t);
+
 /* Float64 brute force of the same step: theta, m, v in double, the bias
  * corrections applied to the moments (m_hat = m/(1-b1^t), v_hat = v/(1-b2^t))
  * and the update theta = theta*(1 - lr*wd) - lr*m_hat/(sqrt(v_hat)+eps).
@@ -99,6 +110,11 @@ float oracle_layer_step(int64_t n, int32_t R, const uint16_t *const *g,
 double oracle_layer_step_f64(int64_t n, int32_t R, const uint16_t *const *g,
                              double *theta, double *m, double *v,
                              const oracle_hparams *hp, int64_t t);
+
+/* The float64 brute force with FP32 gradient replicas. */
+double oracle_layer_step_f64_f32g(int64_t n, int32_t R, const float *const *g,
+                                  double *theta, double *m, double *v,
+                                  const oracle_hparams *hp, int64_t t);
 
 #ifdef __cplusplus
 }

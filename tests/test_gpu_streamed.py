@@ -62,6 +62,21 @@ def init_streamed(S, w, st):
         S.slide_layer_set(st, ui, master=th, step=0)
 
 
+def check_timeline(S, st, sizes):
+    """The engine's per-unit events of the last step are in causal order:
+    copy-in, master landed, copy-in done, update, write-back; the write-back of
+    a unit starts after its update; units are written back in reverse order."""
+    units, fwd_end = S.slide_streamed_timeline(st)
+    assert np.isfinite(fwd_end) and fwd_end >= 0
+    order = ["h2d_begin", "master_landed", "h2d_end", "update_end", "d2h_begin", "d2h_end"]
+    for u in units:
+        vals = [u[k] for k in order]
+        assert all(np.isfinite(vals)), u
+        assert all(a <= b + 1e-3 for a, b in zip(vals, vals[1:])), u
+    ends = [u["d2h_end"] for u in units]
+    assert all(ends[l] >= ends[l + 1] - 1e-3 for l in range(len(units) - 1))
+
+
 def toy(R=3, clip=0.0, seed=5):
     sizes = [5000, 70001, (1 << 20) + 3, 0, 777, 123457]
     return W.Workload("toy", [W.Unit(f"u{i}", [("a", n // 2), ("b", n - n // 2)]) for i, n in enumerate(sizes)],
@@ -97,6 +112,7 @@ def test_streamed_toy_every_element(S, clip, chunk):
                 assert np.array_equal(wb, oracle.f32_to_bf16(a))
                 if clip == 0.0:
                     assert all(r["not_bit_equal"] == 0 for r in rep[:3]), rep
+            check_timeline(S, st, [u.numel for u in w.units])
     finally:
         S.slide_state_destroy(st)
 

@@ -28,8 +28,11 @@ MUTATIONS = {
     "decay_not_scaled_by_lr": ("out->decay = (float)(1.0 - (double)hp->lr * (double)hp->weight_decay);",
                                "out->decay = (float)(1.0 - (double)hp->weight_decay);"),
     "update_sign_flipped": ("th = th - delta;", "th = th + delta;"),
-    "replica_sum_not_mean": ("gm[i] = s / fr;", "gm[i] = s;"),
+    "replica_sum_not_mean": ("s = s + oracle_bf16_to_f32(g[r][i]);\n        gm[i] = s / fr;",
+                             "s = s + oracle_bf16_to_f32(g[r][i]);\n        gm[i] = s;"),
     "replica_index_stuck": ("s = s + oracle_bf16_to_f32(g[r][i]);", "s = s + oracle_bf16_to_f32(g[0][i]);"),
+    "f32_replica_index_stuck": ("            s = s + g[r][i];", "            s = s + g[0][i];"),
+    "f32_replica_sum_not_mean": ("        gm[i] = s / fr;\n    }\n}\n\n/* ---- a2", "        gm[i] = s;\n    }\n}\n\n/* ---- a2"),
     "clip_norm_without_sqrt": ("double norm = sqrt(sqnorm);", "double norm = sqnorm;"),
     "clip_not_clamped": ("if (c > 1.0)\n        c = 1.0;\n    return (float)c;", "return (float)c;"),
     "clip_coef_not_applied": ("float g = gm[i] * coef;", "float g = gm[i];"),

@@ -273,8 +273,9 @@ def test_clip_hand_built():
 
 # --------------------------------------------- library routine: torch ----
 
+@pytest.mark.parametrize("gdt", ["bf16", "f32"])
 @pytest.mark.parametrize("R,clip", [(1, 0.0), (3, 0.0), (4, 1.0), (8, 1e-3)])
-def test_matches_torch_adamw_float64(R, clip):
+def test_matches_torch_adamw_float64(R, clip, gdt):
     """torch.optim.AdamW (decoupled decay, bias correction, eps after the square
     root of the corrected second moment) and torch.nn.utils.clip_grad_norm_
     (coef = c/(norm + 1e-6), clamped at 1), run in float64 on the mean of the
@@ -293,11 +294,12 @@ def test_matches_torch_adamw_float64(R, clip):
     opt = torch.optim.AdamW([p], lr=lr, betas=(b1, b2), eps=eps, weight_decay=wd)
     scales = 10.0 ** rng.uniform(-9, -2, size=n)
     for t in range(1, 21):
-        grads = [oracle.f32_to_bf16((rng.standard_normal(n) * scales).astype(np.float32))
-                 for _ in range(R)]
+        raw = [(rng.standard_normal(n) * scales).astype(np.float32) for _ in range(R)]
+        grads = raw if gdt == "f32" else [oracle.f32_to_bf16(x) for x in raw]
         oracle.layer_step(grads, theta, m, v, None, hp, t)
         oracle.layer_step_f64(grads, th64, m64, v64, hp, t)
-        mean = sum(oracle.bf16_to_f32(g).astype(np.float64) for g in grads) / R
+        vals = raw if gdt == "f32" else [oracle.bf16_to_f32(g) for g in grads]
+        mean = sum(x.astype(np.float64) for x in vals) / R
         p.grad = torch.from_numpy(mean)
         if clip > 0:
             torch.nn.utils.clip_grad_norm_([p], float(np.float32(clip)))
@@ -360,3 +362,55 @@ def test_empty_layer():
     c = oracle.layer_step([np.zeros(0, np.uint16)], theta, theta.copy(), theta.copy(),
                           np.zeros(0, np.uint16), oracle.hparams(max_grad_norm=1.0), 1)
     assert c == 1.0
+
+
+# ---------------------------------------------- FP32 gradient replicas ----
+
+def test_f32_replica_mean_is_elementwise_mean():
+    """FP32 replicas: replica r's element i enters the mean of element i, and
+    the result is the sum divided by R (exact on these small dyadic values)."""
+    rng = np.random.default_rng(55)
+    n = 301
+    k = rng.integers(-30, -10, size=n)            # one exponent per element, shared by the replicas
+    reps = [(rng.integers(-1000, 1001, size=n) * np.exp2(k)).astype(np.float32) for _ in range(4)]
+    gm = oracle.grad_mean(reps)
+    exact = sum(x.astype(np.float64) for x in reps) / 4.0
+    assert np.array_equal(gm.astype(np.float64), exact)
+    gm3 = oracle.grad_mean(reps[:3])
+    ex3 = sum(x.astype(np.float64) for x in reps[:3]) / 3.0
+    assert np.all(np.abs(gm3 - ex3) <= 0.5 * ulp32(ex3))
+
+
+def test_f32_identical_replicas_equal_one_replica():
+    """Values with at most 20 significant bits: every partial sum of up to 8
+    copies (at most 8x) fits in FP32's 24 bits, so the mean equals the single
+    replica bit for bit."""
+    rng = np.random.default_rng(56)
+    n = 2049
+    x = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    x = (x.view(np.uint32) & np.uint32(0xFFFFFFF8)).view(np.float32)   # 20 significant bits
+    th0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    outs = []
+    for reps in (1, 2, 4, 8):
+        th, m, v = th0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+        w = np.zeros(n, np.uint16)
+        for t in range(1, 4):
+            oracle.layer_step([x] * reps, th, m, v, w, oracle.hparams(), t)
+        outs.append((th, m, v, w))
+    for o in outs[1:]:
+        for a, b in zip(outs[0], o):
+            assert np.array_equal(a, b)
+
+
+def test_f32_step1_closed_form():
+    rng = np.random.default_rng(57)
+    n = 3000
+    g = np.concatenate([rng.standard_normal(1000) * 1e-3, rng.standard_normal(1000) * 1e-8,
+                        rng.standard_normal(1000) * 1e-11]).astype(np.float32)
+    th0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    th, m, v = th0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    oracle.layer_step([g], th, m, v, None, oracle.hparams(), 1)
+    lr64, wd64, eps64 = (float(np.float32(a)) for a in (1e-5, 0.01, 1e-8))
+    gv = g.astype(np.float64)
+    want = th0.astype(np.float64) * (1 - lr64 * wd64) - lr64 * gv / (np.abs(gv) + eps64)
+    assert np.all(np.abs(th - want) <= 3 * ulp32(want) + lr64 * 2.0 ** -21)
