@@ -45,10 +45,14 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the FP32-gradient variant leg")
     ap.add_argument("--no-streamed", action="store_true",
                     help="skip the host-streamed leg (8-layer h=8192 model, ~98 GB pinned host memory)")
     ap.add_argument("--streamed-config", type=int, default=5, choices=[4, 5])
     ap.add_argument("--streamed-steps", type=int, default=2)
+    ap.add_argument("--streamed-chunk-mib", type=int, default=64,
+                    help="copy chunk of the streamed engine (the pages' 64 MiB by default)")
     ap.add_argument("--batches", type=int, default=4,
                     help="pre-generated gradient batches cycled by the steps (1 for small profiling runs)")
     ap.add_argument("--soak-s", type=float, default=1.5,
@@ -214,6 +218,62 @@ def run_reference(args):
     return 0
 
 
+# ------------------------------------------------- FP32-gradient variant ----
+
+def run_fp32_variant(args, S, torch, synth, peak):
+    """The same workload with FP32 gradient replicas (26 + 4R bytes per
+    parameter in the fused kernel, 4R in the clip pre-pass), timed like the
+    main line: per-launch events, back to back, inputs larger than L2."""
+    from synth import workloads as W
+    w = W.config2_fp32()
+    n, R = w.units[0].numel, w.R
+    clip = w.max_grad_norm > 0
+    hp = S.hparams(*w.hparams_tuple())
+    stream = torch.cuda.Stream()
+    st = S.slide_state_create([n], R, flags=S.SLIDE_FLAG_FP32_GRADS)
+    try:
+        synth.dev_master(S.slide_layer_ptrs(st, 0)[0], n, w.seed, stream=stream.cuda_stream)
+        batches = []
+        for b in range(2):
+            reps = [torch.empty(n + 64, dtype=torch.float32, device="cuda") for _ in range(R)]
+            for r, t in enumerate(reps):
+                synth.dev_grad_f32(t.data_ptr(), n, synth.spec(w.seed), 0, b + 1, r, w.grad_scale,
+                                   stream=stream.cuda_stream)
+            batches.append(reps)
+        torch.cuda.synchronize()
+        for i in range(max(3, args.warmup)):
+            S.slide_layer_step(st, 0, batches[i % 2], hp, stream)
+        K = min(args.steps, 500)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+        for trio in ev:
+            for e in trio:
+                e.record(stream)
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for k in range(K):
+            S.slide_trace_events(st, ev[k][0], ev[k][1], ev[k][2])
+            S.slide_layer_step(st, 0, batches[k % 2], hp, stream)
+        stop.record(stream)
+        torch.cuda.synchronize()
+        S.slide_trace_events(st)
+        ms = start.elapsed_time(stop)
+        upd = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
+        pre = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    finally:
+        S.slide_state_destroy(st)
+    b_upd, b_pre = (26 + 4 * R) * n, (4 * R * n if clip else 0)
+    return {"workload": w.name, "description": w.description, "steps": K, "value": n * K / (ms * 1e-3) / 1e9,
+            "unit": UNIT, "ms_per_step": ms / K,
+            "roofline": {"bound": "hbm", "kernel": "grad_reduce_adamw_cast (FP32 replicas)",
+                         "achieved": b_upd / (upd * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+                         "frac": b_upd / (upd * 1e-3) / 1e9 / peak, "bytes_per_param": 26 + 4 * R,
+                         "avg_launch_ms": upd},
+            "prepass": {"achieved": b_pre / (pre * 1e-3) / 1e9 if clip else None, "avg_launch_ms": pre,
+                        "bytes_per_param": 4 * R},
+            "step_roofline_frac": (b_upd + b_pre) / (ms / K * 1e-3) / 1e9 / peak}
+
+
 # ----------------------------------------------------------- streamed ----
 
 def kernel_source_sha256():
@@ -344,7 +404,8 @@ def run_streamed(args, S, torch, synth):
     mg = synth.ModelGrads(sp, len(sizes), w.R, 1, 0, C.cast(numel, C.c_void_p), None, None, None, None,
                           w.grad_scale)
     t0 = time.time()
-    st = S.slide_state_create(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED)
+    st = S.slide_state_create(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED,
+                              chunk_bytes=args.streamed_chunk_mib << 20)
     create_s = time.time() - t0
     try:
         for ui, u in enumerate(w.units):
@@ -379,7 +440,7 @@ def run_streamed(args, S, torch, synth):
             "link_bytes_per_step": {"h2d": 14 * N, "d2h": 14 * N},
             "achieved_link_gbs_each_way": 14 * N / s_step / 1e9,
             "link": link, "host_pinned_gb": host_b / 1e9, "window_gb": dev_b / 1e9,
-            "create_s": create_s,
+            "create_s": create_s, "chunk_mib": args.streamed_chunk_mib,
             "grad_callback": f"copies pre-generated replicas ({n_pool} sets, the workload's distribution) "
                              "from HBM into the window",
             "s_per_step_with_generator_callback": gen_s,
@@ -539,6 +600,9 @@ def run_ours(args):
     finally:
         S.slide_state_destroy(st)
 
+    variant = None
+    if not args.no_variants and world == 1:
+        variant = run_fp32_variant(args, S, torch, synth, measured_peaks()[0])
     streamed = None
     if not args.no_streamed and world == 1:
         streamed = run_streamed(args, S, torch, synth)
@@ -601,6 +665,7 @@ def run_ours(args):
         "clocks": clocks,
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "fp32_grad_variant": variant,
         "streamed": streamed,
     }
     print(json.dumps(line), flush=True)

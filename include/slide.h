@@ -4,7 +4,8 @@
  *
  * What the step computes (the pages print no update equation; the reading is
  * stated here once and used by every entry point):
- *   for each parameter i of layer l, with R gradient replicas g_r (BF16) and
+ *   for each parameter i of layer l, with R gradient replicas g_r (BF16, or
+ *   FP32 with SLIDE_FLAG_FP32_GRADS) and
  *   the layer's own 1-based update count t:
  *     g   = (sum_r g_r[i], in FP32, replica order) / R       -- replica mean
  *     g  *= min(1, c / (||g||_2 + 1e-6))   if c = max_grad_norm > 0,
@@ -89,10 +90,13 @@ enum {
 
 enum {
     SLIDE_FLAG_CHECK_FINITE = 1u,       /* check the mean gradient for NaN/Inf each step */
-    SLIDE_FLAG_TEST_PIPELINE_STALL = 2u /* tests only: the update kernel's copy producer issues nothing,
-                                           so the consumers' bounded wait (2 s) runs out and the step
-                                           reports SLIDE_ERR_TIMEOUT through slide_layer_status; the
-                                           layer's values are then undefined */
+    SLIDE_FLAG_TEST_PIPELINE_STALL = 2u, /* tests only: the update kernel's copy producer issues nothing,
+                                            so the consumers' bounded wait (2 s) runs out and the step
+                                            reports SLIDE_ERR_TIMEOUT through slide_layer_status; the
+                                            layer's values are then undefined */
+    SLIDE_FLAG_FP32_GRADS = 4u           /* the R gradient replicas are FP32 (FP32 gradient
+                                            accumulation), not BF16: every replica pointer then holds
+                                            n floats, and the step moves 26 + 4R bytes per parameter */
 };
 
 /* Adam hyper-parameters (FP32).  Valid: lr >= 0, 0 <= beta1 < 1,

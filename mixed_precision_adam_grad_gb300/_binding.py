@@ -35,6 +35,7 @@ SLIDE_RESIDENCY_HBM = 0
 SLIDE_RESIDENCY_HOST_STREAMED = 1
 SLIDE_FLAG_CHECK_FINITE = 1
 SLIDE_FLAG_TEST_PIPELINE_STALL = 2
+SLIDE_FLAG_FP32_GRADS = 4
 SLIDE_MAX_REPLICAS = 8
 
 

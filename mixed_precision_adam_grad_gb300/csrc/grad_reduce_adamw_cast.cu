@@ -9,7 +9,8 @@
 // cores onto the GPU and fused into one kernel.
 //
 // The step is elementwise and bandwidth-bound ((26 + 2R) bytes and ~20 FP32
-// operations per parameter), so no tensor cores.  The kernel is a persistent
+// operations per parameter with BF16 replicas, 26 + 4R with FP32 replicas),
+// so no tensor cores.  The kernel is a persistent
 // producer/consumer pipeline, one CTA per SM:
 //  - one producer thread streams tiles of kTile parameters of every input
 //    (R replicas, master, m, v) into a kStages-deep shared-memory ring with
@@ -126,16 +127,58 @@ __device__ __forceinline__ uint32_t pack_bf16x2(uint16_t lo, uint16_t hi)
     return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
-// Mean gradient of parameter e (0..3) of a 4-wide group, from R 8-byte words.
-template <int R, bool CLIP, bool CHECK>
-__device__ __forceinline__ float mean_of(const uint2 (&gw)[R], int e, float coef, bool &bad)
+// Gradient element types: BF16 replicas (bit patterns in uint16_t) or FP32
+// replicas.  V4 holds 4 consecutive values; at() widens one of them to FP32.
+template <typename G>
+struct GradT;
+
+template <>
+struct GradT<uint16_t> {
+    using V4 = uint2;
+    static __device__ __forceinline__ float at(const uint2 &v, int e)
+    {
+        const uint32_t word = (e < 2) ? v.x : v.y;
+        return (e & 1) ? bf16_hi(word) : bf16_lo(word);
+    }
+    static __device__ __forceinline__ float one(const uint16_t *p, int64_t i)
+    {
+        return __uint_as_float((uint32_t)p[i] << 16);
+    }
+    // the 8 values of vector k (16 bytes)
+    static __device__ __forceinline__ void load8(const void *base, int64_t k, float (&x)[8])
+    {
+        const uint4 q = __ldcs(reinterpret_cast<const uint4 *>(base) + k);
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            x[e] = (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]);
+    }
+};
+
+template <>
+struct GradT<float> {
+    using V4 = float4;
+    static __device__ __forceinline__ float at(const float4 &v, int e)
+    {
+        return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+    }
+    static __device__ __forceinline__ float one(const float *p, int64_t i) { return p[i]; }
+    static __device__ __forceinline__ void load8(const void *base, int64_t k, float (&x)[8])
+    {
+        const float4 a = __ldcs(reinterpret_cast<const float4 *>(base) + 2 * k);
+        const float4 b = __ldcs(reinterpret_cast<const float4 *>(base) + 2 * k + 1);
+        x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+    }
+};
+
+// Mean gradient of parameter e (0..3) of a 4-wide group, from R 4-value vectors.
+template <typename G, int R, bool CLIP, bool CHECK>
+__device__ __forceinline__ float mean_of(const typename GradT<G>::V4 (&gw)[R], int e, float coef, bool &bad)
 {
     float x[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const uint32_t word = (e < 2) ? gw[r].x : gw[r].y;
-        x[r] = (e & 1) ? bf16_hi(word) : bf16_lo(word);
-    }
+    for (int r = 0; r < R; ++r)
+        x[r] = GradT<G>::at(gw[r], e);
     float g = replica_mean<R>(x);
     if constexpr (CHECK)
         bad |= !isfinite(g);
@@ -145,9 +188,10 @@ __device__ __forceinline__ float mean_of(const uint2 (&gw)[R], int e, float coef
 }
 
 // Update 4 consecutive parameters held in registers and store them.
-template <int R, bool CLIP, bool CHECK>
-__device__ __forceinline__ void update4_store(const uint2 (&gw)[R], float4 th, float4 mm, float4 vv, int64_t e0,
-                                              const KArgs &a, const AdamScalars &s, float coef, bool &bad)
+template <typename G, int R, bool CLIP, bool CHECK>
+__device__ __forceinline__ void update4_store(const typename GradT<G>::V4 (&gw)[R], float4 th, float4 mm,
+                                              float4 vv, int64_t e0, const KArgs &a, const AdamScalars &s,
+                                              float coef, bool &bad)
 {
     float t[4] = {th.x, th.y, th.z, th.w};
     float m[4] = {mm.x, mm.y, mm.z, mm.w};
@@ -155,7 +199,7 @@ __device__ __forceinline__ void update4_store(const uint2 (&gw)[R], float4 th, f
     uint16_t w[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e)
-        adamw_one(mean_of<R, CLIP, CHECK>(gw, e, coef, bad), t[e], m[e], v[e], w[e], s);
+        adamw_one(mean_of<G, R, CLIP, CHECK>(gw, e, coef, bad), t[e], m[e], v[e], w[e], s);
     __stcs(reinterpret_cast<float4 *>(a.theta + e0), make_float4(t[0], t[1], t[2], t[3]));
     __stcs(reinterpret_cast<float4 *>(a.m + e0), make_float4(m[0], m[1], m[2], m[3]));
     __stcs(reinterpret_cast<float4 *>(a.v + e0), make_float4(v[0], v[1], v[2], v[3]));
@@ -258,18 +302,19 @@ __device__ __forceinline__ void bulk_load(void *dst_smem, const void *src_gmem, 
         : "memory");
 }
 
-template <int R>
+template <typename G, int R>
 struct Pipe {
-    static constexpr uint32_t kGradBytes = kTile * 2;
+    static constexpr uint32_t kGradBytes = kTile * sizeof(G);
     static constexpr uint32_t kF32Bytes = kTile * 4;
     static constexpr uint32_t kStageBytes = R * kGradBytes + 3 * kF32Bytes;
     static constexpr uint32_t kSmemBytes = kStages * kStageBytes + 2 * kStages * 8;
 };
 
-template <int R, bool CLIP, bool CHECK>
+template <typename G, int R, bool CLIP, bool CHECK>
 __global__ void __launch_bounds__(kPipeThreads, 1) k_grad_reduce_adamw_cast(KArgs a)
 {
-    using P = Pipe<R>;
+    using P = Pipe<G, R>;
+    using V4 = typename GradT<G>::V4;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * P::kStageBytes);
     uint64_t *empty = full + kStages;
@@ -314,7 +359,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_grad_reduce_adamw_cast(KArg
             const int64_t e0 = tile * kTile;
 #pragma unroll
             for (int r = 0; r < R; ++r)
-                bulk_load(base + r * P::kGradBytes, static_cast<const uint16_t *>(a.g.p[r]) + e0, P::kGradBytes,
+                bulk_load(base + r * P::kGradBytes, static_cast<const G *>(a.g.p[r]) + e0, P::kGradBytes,
                           &full[stage]);
             bulk_load(base + R * P::kGradBytes, a.theta + e0, P::kF32Bytes, &full[stage]);
             bulk_load(base + R * P::kGradBytes + P::kF32Bytes, a.m + e0, P::kF32Bytes, &full[stage]);
@@ -349,12 +394,12 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_grad_reduce_adamw_cast(KArg
             break;
         }
         const unsigned char *base = smem + stage * P::kStageBytes;
-        uint2 g0[R], g1[R];
+        V4 g0[R], g1[R];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             const unsigned char *gb = base + r * P::kGradBytes;
-            g0[r] = *reinterpret_cast<const uint2 *>(gb + c * 8);
-            g1[r] = *reinterpret_cast<const uint2 *>(gb + kTile + c * 8);
+            g0[r] = *reinterpret_cast<const V4 *>(gb + c * sizeof(V4));
+            g1[r] = *reinterpret_cast<const V4 *>(gb + P::kGradBytes / 2 + c * sizeof(V4));
         }
         const unsigned char *fb = base + R * P::kGradBytes;
         const float4 t0 = *reinterpret_cast<const float4 *>(fb + c * 16);
@@ -367,8 +412,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_grad_reduce_adamw_cast(KArg
         if (lane == 0)
             mbar_arrive(&empty[stage]);
         const int64_t e0 = tile * kTile + 4 * c;
-        update4_store<R, CLIP, CHECK>(g0, t0, m0, v0, e0, a, s, coef, bad);
-        update4_store<R, CLIP, CHECK>(g1, t1, m1, v1, e0 + kTile / 2, a, s, coef, bad);
+        update4_store<G, R, CLIP, CHECK>(g0, t0, m0, v0, e0, a, s, coef, bad);
+        update4_store<G, R, CLIP, CHECK>(g1, t1, m1, v1, e0 + kTile / 2, a, s, coef, bad);
         if (++stage == kStages) {
             stage = 0;
             phase ^= 1u;
@@ -382,14 +427,14 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_grad_reduce_adamw_cast(KArg
         const int64_t groups = rem >> 2;            // 4-wide groups, < 512
         for (int64_t q = c; q < groups; q += kConsumerWarps * 32) {
             const int64_t e0 = base_e + 4 * q;
-            uint2 gw[R];
+            V4 gw[R];
 #pragma unroll
             for (int r = 0; r < R; ++r)
-                gw[r] = __ldcs(reinterpret_cast<const uint2 *>(static_cast<const uint16_t *>(a.g.p[r]) + e0));
+                gw[r] = __ldcs(reinterpret_cast<const V4 *>(static_cast<const G *>(a.g.p[r]) + e0));
             const float4 t = __ldcs(reinterpret_cast<const float4 *>(a.theta + e0));
             const float4 m = __ldcs(reinterpret_cast<const float4 *>(a.m + e0));
             const float4 v = __ldcs(reinterpret_cast<const float4 *>(a.v + e0));
-            update4_store<R, CLIP, CHECK>(gw, t, m, v, e0, a, s, coef, bad);
+            update4_store<G, R, CLIP, CHECK>(gw, t, m, v, e0, a, s, coef, bad);
         }
         const int64_t tail0 = base_e + (groups << 2);
         if (c < a.n - tail0) {
@@ -397,7 +442,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_grad_reduce_adamw_cast(KArg
             float x[R];
 #pragma unroll
             for (int r = 0; r < R; ++r)
-                x[r] = __uint_as_float((uint32_t)static_cast<const uint16_t *>(a.g.p[r])[i] << 16);
+                x[r] = GradT<G>::one(static_cast<const G *>(a.g.p[r]), i);
             float g = replica_mean<R>(x);
             if constexpr (CHECK)
                 bad |= !isfinite(g);
@@ -452,7 +497,7 @@ struct SqArgs {
     double *partials;
 };
 
-template <int R, int UNROLL>
+template <typename G, int R, int UNROLL>
 __global__ void __launch_bounds__(kThreads) k_grad_sqnorm(SqArgs a)
 {
     const int64_t nvec = a.n >> 3;
@@ -460,14 +505,14 @@ __global__ void __launch_bounds__(kThreads) k_grad_sqnorm(SqArgs a)
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     SqAcc acc;
     for (int64_t k0 = tid; k0 < nvec; k0 += stride * UNROLL) {
-        uint4 gv[UNROLL][R];
+        float xv[UNROLL][R][8];
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const int64_t k = k0 + (int64_t)u * stride;
             if (k < nvec) {
 #pragma unroll
                 for (int r = 0; r < R; ++r)
-                    gv[u][r] = __ldcs(reinterpret_cast<const uint4 *>(a.g.p[r]) + k);
+                    GradT<G>::load8(a.g.p[r], k, xv[u][r]);
             }
         }
 #pragma unroll
@@ -478,10 +523,8 @@ __global__ void __launch_bounds__(kThreads) k_grad_sqnorm(SqArgs a)
                 for (int e = 0; e < 8; ++e) {
                     float x[R];
 #pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const uint32_t word = (&gv[u][r].x)[e >> 1];
-                        x[r] = (e & 1) ? bf16_hi(word) : bf16_lo(word);
-                    }
+                    for (int r = 0; r < R; ++r)
+                        x[r] = xv[u][r][e];
                     acc.add(replica_mean<R>(x));
                 }
             }
@@ -492,10 +535,8 @@ __global__ void __launch_bounds__(kThreads) k_grad_sqnorm(SqArgs a)
         const int64_t i = tail0 + tid;
         float x[R];
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const uint16_t h = reinterpret_cast<const uint16_t *>(a.g.p[r])[i];
-            x[r] = __uint_as_float((uint32_t)h << 16);
-        }
+        for (int r = 0; r < R; ++r)
+            x[r] = GradT<G>::one(static_cast<const G *>(a.g.p[r]), i);
         acc.add(replica_mean<R>(x));
     }
 
@@ -568,11 +609,12 @@ unsigned grid_for(int device, int64_t n, int cap)
 
 constexpr int kUnrollSq = 2;
 
-template <int R, bool CLIP, bool CHECK>
+template <typename G, int R, bool CLIP, bool CHECK>
 cudaError_t launch_step_r(const KArgs &a, int device, cudaStream_t stream)
 {
-    constexpr auto kern = k_grad_reduce_adamw_cast<R, CLIP, CHECK>;
-    constexpr uint32_t smem = Pipe<R>::kSmemBytes;
+    constexpr auto kern = k_grad_reduce_adamw_cast<G, R, CLIP, CHECK>;
+    constexpr uint32_t smem = Pipe<G, R>::kSmemBytes;
+    static_assert(smem <= 227 * 1024, "pipeline stages exceed the shared memory of a CTA");
     static int attr_set[64] = {0};
     if (device >= 0 && device < 64 && !attr_set[device]) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -589,20 +631,36 @@ cudaError_t launch_step_r(const KArgs &a, int device, cudaStream_t stream)
     return cudaGetLastError();
 }
 
-template <int R>
+template <typename G, int R>
 cudaError_t launch_step_flags(const KArgs &a, bool clip, bool check, int device, cudaStream_t stream)
 {
     if (clip)
-        return check ? launch_step_r<R, true, true>(a, device, stream)
-                     : launch_step_r<R, true, false>(a, device, stream);
-    return check ? launch_step_r<R, false, true>(a, device, stream)
-                 : launch_step_r<R, false, false>(a, device, stream);
+        return check ? launch_step_r<G, R, true, true>(a, device, stream)
+                     : launch_step_r<G, R, true, false>(a, device, stream);
+    return check ? launch_step_r<G, R, false, true>(a, device, stream)
+                 : launch_step_r<G, R, false, false>(a, device, stream);
 }
 
-template <int R>
+template <typename G>
+cudaError_t launch_step_g(const KArgs &a, int R, bool clip, bool check, int device, cudaStream_t stream)
+{
+    switch (R) {
+    case 1: return launch_step_flags<G, 1>(a, clip, check, device, stream);
+    case 2: return launch_step_flags<G, 2>(a, clip, check, device, stream);
+    case 3: return launch_step_flags<G, 3>(a, clip, check, device, stream);
+    case 4: return launch_step_flags<G, 4>(a, clip, check, device, stream);
+    case 5: return launch_step_flags<G, 5>(a, clip, check, device, stream);
+    case 6: return launch_step_flags<G, 6>(a, clip, check, device, stream);
+    case 7: return launch_step_flags<G, 7>(a, clip, check, device, stream);
+    case 8: return launch_step_flags<G, 8>(a, clip, check, device, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename G, int R>
 cudaError_t launch_sq_r(const SqArgs &a, int *n_partials, int device, cudaStream_t stream)
 {
-    constexpr auto kern = k_grad_sqnorm<R, kUnrollSq>;
+    constexpr auto kern = k_grad_sqnorm<G, R, kUnrollSq>;
     unsigned grid = grid_for<kern>(device, a.n, kMaxPartials);
     kern<<<grid, kThreads, 0, stream>>>(a);
     *n_partials = (int)grid;
@@ -646,27 +704,35 @@ cudaError_t launch_cast_bf16(const float *src, uint16_t *w, int64_t n, cudaStrea
     return cudaGetLastError();
 }
 
-cudaError_t launch_grad_sqnorm(const ReplicaPtrs &g, int R, int64_t n, const ClipScratch &scratch,
-                               int *n_partials, int device, cudaStream_t stream)
+template <typename G>
+cudaError_t launch_sq_g(const SqArgs &a, int R, int *n_partials, int device, cudaStream_t stream)
 {
-    SqArgs a{g, n, scratch.partials};
     switch (R) {
-    case 1: return launch_sq_r<1>(a, n_partials, device, stream);
-    case 2: return launch_sq_r<2>(a, n_partials, device, stream);
-    case 3: return launch_sq_r<3>(a, n_partials, device, stream);
-    case 4: return launch_sq_r<4>(a, n_partials, device, stream);
-    case 5: return launch_sq_r<5>(a, n_partials, device, stream);
-    case 6: return launch_sq_r<6>(a, n_partials, device, stream);
-    case 7: return launch_sq_r<7>(a, n_partials, device, stream);
-    case 8: return launch_sq_r<8>(a, n_partials, device, stream);
+    case 1: return launch_sq_r<G, 1>(a, n_partials, device, stream);
+    case 2: return launch_sq_r<G, 2>(a, n_partials, device, stream);
+    case 3: return launch_sq_r<G, 3>(a, n_partials, device, stream);
+    case 4: return launch_sq_r<G, 4>(a, n_partials, device, stream);
+    case 5: return launch_sq_r<G, 5>(a, n_partials, device, stream);
+    case 6: return launch_sq_r<G, 6>(a, n_partials, device, stream);
+    case 7: return launch_sq_r<G, 7>(a, n_partials, device, stream);
+    case 8: return launch_sq_r<G, 8>(a, n_partials, device, stream);
     default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_grad_sqnorm(const ReplicaPtrs &g, int R, int64_t n, const ClipScratch &scratch,
+                               int *n_partials, int device, cudaStream_t stream, bool f32_grads)
+{
+    SqArgs a{g, n, scratch.partials};
+    return f32_grads ? launch_sq_g<float>(a, R, n_partials, device, stream)
+                     : launch_sq_g<uint16_t>(a, R, n_partials, device, stream);
 }
 
 cudaError_t launch_grad_reduce_adamw_cast(const ReplicaPtrs &g, int R, int64_t n, float *theta,
                                           float *m, float *v, uint16_t *w, const AdamScalars &s,
                                           const ClipScratch *clip, int n_partials, float max_norm,
-                                          bool check_finite, int device, cudaStream_t stream, bool test_stall)
+                                          bool check_finite, int device, cudaStream_t stream, bool test_stall,
+                                          bool f32_grads)
 {
     const bool do_clip = clip != nullptr && clip->partials != nullptr && max_norm > 0.0f;
     KArgs a{};
@@ -683,17 +749,8 @@ cudaError_t launch_grad_reduce_adamw_cast(const ReplicaPtrs &g, int R, int64_t n
     a.coef_out = do_clip ? clip->coef : nullptr;
     a.status = clip ? clip->status : nullptr;
     a.test_stall = test_stall ? 1 : 0;
-    switch (R) {
-    case 1: return launch_step_flags<1>(a, do_clip, check_finite, device, stream);
-    case 2: return launch_step_flags<2>(a, do_clip, check_finite, device, stream);
-    case 3: return launch_step_flags<3>(a, do_clip, check_finite, device, stream);
-    case 4: return launch_step_flags<4>(a, do_clip, check_finite, device, stream);
-    case 5: return launch_step_flags<5>(a, do_clip, check_finite, device, stream);
-    case 6: return launch_step_flags<6>(a, do_clip, check_finite, device, stream);
-    case 7: return launch_step_flags<7>(a, do_clip, check_finite, device, stream);
-    case 8: return launch_step_flags<8>(a, do_clip, check_finite, device, stream);
-    default: return cudaErrorInvalidValue;
-    }
+    return f32_grads ? launch_step_g<float>(a, R, do_clip, check_finite, device, stream)
+                     : launch_step_g<uint16_t>(a, R, do_clip, check_finite, device, stream);
 }
 
 }  // namespace slide

@@ -94,7 +94,7 @@ static slide_status check_config(const slide_config *cfg, int64_t *max_numel)
         return fail(SLIDE_ERR_INVALID_ARG, "config: window_layers must be 2 (or 0 for the default 2)");
     if (cfg->chunk_bytes < 0 || (cfg->chunk_bytes % 256) != 0)
         return fail(SLIDE_ERR_INVALID_ARG, "config: chunk_bytes must be a non-negative multiple of 256");
-    if (cfg->flags & ~(uint32_t)(SLIDE_FLAG_CHECK_FINITE | SLIDE_FLAG_TEST_PIPELINE_STALL))
+    if (cfg->flags & ~(uint32_t)(SLIDE_FLAG_CHECK_FINITE | SLIDE_FLAG_TEST_PIPELINE_STALL | SLIDE_FLAG_FP32_GRADS))
         return fail(SLIDE_ERR_INVALID_ARG, "config: unknown flag bits");
     if (cfg->device < 0)
         return fail(SLIDE_ERR_INVALID_ARG, "config: device < 0");
@@ -329,8 +329,9 @@ slide_status slide_layer_step(slide_state *st, int32_t layer, const void *const 
         cudaError_t e;
         if (st->trace[0])
             cudaEventRecord(st->trace[0], s);
+        const bool f32g = (st->cfg.flags & SLIDE_FLAG_FP32_GRADS) != 0;
         if (clip) {
-            e = launch_grad_sqnorm(g, R, L.n, L.scratch, &n_partials, st->device, s);
+            e = launch_grad_sqnorm(g, R, L.n, L.scratch, &n_partials, st->device, s, f32g);
             if (e != cudaSuccess)
                 return fail_cuda(e, "grad_sqnorm launch");
         }
@@ -338,7 +339,7 @@ slide_status slide_layer_step(slide_state *st, int32_t layer, const void *const 
             cudaEventRecord(st->trace[1], s);
         e = launch_grad_reduce_adamw_cast(g, R, L.n, L.theta, L.m, L.v, w, sc, &L.scratch, n_partials,
                                           clip ? hp->max_grad_norm : 0.0f, check, st->device, s,
-                                          (st->cfg.flags & SLIDE_FLAG_TEST_PIPELINE_STALL) != 0);
+                                          (st->cfg.flags & SLIDE_FLAG_TEST_PIPELINE_STALL) != 0, f32g);
         if (e != cudaSuccess)
             return fail_cuda(e, "grad_reduce_adamw_cast launch");
         if (st->trace[2])

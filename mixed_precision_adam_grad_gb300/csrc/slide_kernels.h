@@ -31,10 +31,12 @@ struct ClipScratch {
     unsigned *status;  // bit 0: a non-finite mean gradient was seen
 };
 
+// Replicas are BF16 (uint16_t bit patterns) unless f32_grads, then FP32.
+//
 // Clip pre-pass: per-block partial sums of the squared replica mean into
 // scratch.partials; returns the number of partials written via *n_partials.
 cudaError_t launch_grad_sqnorm(const ReplicaPtrs &g, int R, int64_t n, const ClipScratch &scratch,
-                               int *n_partials, int device, cudaStream_t stream);
+                               int *n_partials, int device, cudaStream_t stream, bool f32_grads = false);
 
 // Fused step.  When max_norm > 0 the kernel reduces the n_partials partial
 // sums (in a fixed order, identically in every block) to the clip coefficient.
@@ -44,7 +46,7 @@ cudaError_t launch_grad_reduce_adamw_cast(const ReplicaPtrs &g, int R, int64_t n
                                           float *m, float *v, uint16_t *w, const AdamScalars &s,
                                           const ClipScratch *clip, int n_partials, float max_norm,
                                           bool check_finite, int device, cudaStream_t stream,
-                                          bool test_stall = false);
+                                          bool test_stall = false, bool f32_grads = false);
 
 // w[i] = bf16_rne(src[i]) (used when a caller overwrites a master copy).
 cudaError_t launch_cast_bf16(const float *src, uint16_t *w, int64_t n, cudaStream_t stream);

@@ -63,16 +63,19 @@ constexpr int kRegions = 3;  // master, m, v (the arrays the next copy-in overwr
 struct Slot {
     float *arr[kRegions] = {nullptr, nullptr, nullptr};  // master, m, v
     uint16_t *w = nullptr;
-    uint16_t *g[kMaxReplicas] = {};
+    void *g[kMaxReplicas] = {};
     ClipScratch scratch{};
     // chunk k of region r freed by the D2H of the unit that used this slot last
     std::vector<cudaEvent_t> freed[kRegions];
     cudaEvent_t w_freed = nullptr;  // D2H of the BF16 copy done
 };
 
-size_t slot_bytes(int64_t maxn, int R)
+size_t grad_bytes(const slide_config &cfg) { return (cfg.flags & SLIDE_FLAG_FP32_GRADS) ? 4 : 2; }
+
+size_t slot_bytes(int64_t maxn, int R, size_t gsize)
 {
-    return 3 * align_up((size_t)maxn * 4) + align_up((size_t)maxn * 2) * (1 + (size_t)R) + scratch_bytes();
+    return 3 * align_up((size_t)maxn * 4) + align_up((size_t)maxn * 2) +
+           align_up((size_t)maxn * gsize) * (size_t)R + scratch_bytes();
 }
 
 }  // namespace
@@ -98,7 +101,7 @@ struct StreamEngine {
 
 size_t engine_device_bytes(const slide_config &cfg, int64_t max_numel)
 {
-    return kSlots * slot_bytes(max_numel, cfg.n_replicas);
+    return kSlots * slot_bytes(max_numel, cfg.n_replicas, grad_bytes(cfg));
 }
 
 static void destroy_engine_objects(StreamEngine *E)
@@ -169,8 +172,8 @@ slide_status engine_create(slide_state *st)
         s.w = (uint16_t *)p;
         p += align_up((size_t)maxn * 2);
         for (int r = 0; r < R; ++r) {
-            s.g[r] = (uint16_t *)p;
-            p += align_up((size_t)maxn * 2);
+            s.g[r] = p;
+            p += align_up((size_t)maxn * grad_bytes(st->cfg));
         }
         s.scratch.partials = (double *)p;
         s.scratch.coef = (float *)(p + align_up(sizeof(double) * kMaxPartials));
@@ -375,14 +378,16 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
             for (int r = 0; r < R; ++r)
                 g.p[r] = s.g[r];
             int n_partials = 0;
+            const bool f32g = (st->cfg.flags & SLIDE_FLAG_FP32_GRADS) != 0;
             if (clip) {
-                e = launch_grad_sqnorm(g, R, U.n, s.scratch, &n_partials, st->device, E->s_comp);
+                e = launch_grad_sqnorm(g, R, U.n, s.scratch, &n_partials, st->device, E->s_comp, f32g);
                 if (e != cudaSuccess)
                     break;
             }
             e = launch_grad_reduce_adamw_cast(g, R, U.n, s.arr[0], s.arr[1], s.arr[2], s.w, sc, &s.scratch,
                                               n_partials, clip ? hp.max_grad_norm : 0.0f, check, st->device,
-                                              E->s_comp);
+                                              E->s_comp, (st->cfg.flags & SLIDE_FLAG_TEST_PIPELINE_STALL) != 0,
+                                              f32g);
             if (e != cudaSuccess)
                 break;
         }

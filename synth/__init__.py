@@ -39,13 +39,13 @@ class ModelGrads(C.Structure):
                 ("step", C.c_uint32), ("unit_id_base", C.c_uint32),
                 ("unit_numel", C.c_void_p), ("seg_begin", C.c_void_p),
                 ("seg_offset", C.c_void_p), ("seg_len", C.c_void_p),
-                ("seg_scale", C.c_void_p), ("default_scale", C.c_float)]
+                ("seg_scale", C.c_void_p), ("default_scale", C.c_float), ("fp32_grads", C.c_int32)]
 
 
 class PoolGrads(C.Structure):
     """User data of the pool-copy gradient callback."""
     _fields_ = [("n_replicas", C.c_int32), ("n_pool", C.c_int32), ("step", C.c_uint32),
-                ("pad_", C.c_int32), ("unit_numel", C.c_void_p), ("pool", C.c_void_p)]
+                ("fp32_grads", C.c_int32), ("unit_numel", C.c_void_p), ("pool", C.c_void_p)]
 
 
 def _stale(so, srcs):
@@ -90,6 +90,8 @@ def host():
         L.syn_host_fill_grad.argtypes = [P, i64, i64, C.POINTER(GradSpec), u32, u32, u32, C.c_float]
         L.syn_host_gather_master.argtypes = [P, P, i64, u32, u32, C.c_float]
         L.syn_host_gather_grad.argtypes = [P, P, i64, C.POINTER(GradSpec), u32, u32, u32, C.c_float]
+        L.syn_host_fill_grad_f32.argtypes = [P, i64, i64, C.POINTER(GradSpec), u32, u32, u32, C.c_float]
+        L.syn_host_gather_grad_f32.argtypes = [P, P, i64, C.POINTER(GradSpec), u32, u32, u32, C.c_float]
         L.syn_host_uniform.restype = C.c_float
         L.syn_host_uniform.argtypes = [u32, u32, u32, u32, u32, C.c_uint64]
         L.syn_host_philox.argtypes = [P, P, P]
@@ -107,6 +109,7 @@ def dev():
         L.syn_dev_fill_master.argtypes = [P, i64, i64, u32, u32, C.c_float, P]
         L.syn_dev_fill_grad.argtypes = [P, i64, i64, C.POINTER(GradSpec), u32, u32, u32, C.c_float, P]
         L.syn_dev_normals.argtypes = [P, i64, u32, u32, u32, u32, u32, P]
+        L.syn_dev_fill_grad_f32.argtypes = [P, i64, i64, C.POINTER(GradSpec), u32, u32, u32, C.c_float, P]
         L.syn_dev_grad_fn.argtypes = [P, C.c_int32, P, P]
         L.syn_dev_pool_grad_fn.argtypes = [P, C.c_int32, P, P]
         _dev = L
@@ -159,6 +162,21 @@ def grad(n, sp: GradSpec, unit, step, replica, scale, offset=0) -> np.ndarray:
     return out
 
 
+def grad_f32(n, sp: GradSpec, unit, step, replica, scale, offset=0) -> np.ndarray:
+    """FP32 gradient replica values (before any BF16 rounding)."""
+    out = np.empty(n, np.float32)
+    host().syn_host_fill_grad_f32(out.ctypes.data, n, offset, C.byref(sp), unit, step, replica, scale)
+    return out
+
+
+def gather_grad_f32(idx, sp: GradSpec, unit, step, replica, scale) -> np.ndarray:
+    idx = np.ascontiguousarray(idx, np.int64)
+    out = np.empty(idx.size, np.float32)
+    host().syn_host_gather_grad_f32(out.ctypes.data, idx.ctypes.data, idx.size, C.byref(sp), unit, step,
+                                    replica, scale)
+    return out
+
+
 def gather_master(idx, seed, unit=0, scale=0.02) -> np.ndarray:
     idx = np.ascontiguousarray(idx, np.int64)
     out = np.empty(idx.size, np.float32)
@@ -188,6 +206,11 @@ def dev_master(ptr, n, seed, unit=0, scale=0.02, offset=0, stream=0):
 def dev_grad(ptr, n, sp: GradSpec, unit, step, replica, scale, offset=0, stream=0):
     _check(dev().syn_dev_fill_grad(ptr, n, offset, C.byref(sp), unit, step, replica, scale, stream),
            "syn_dev_fill_grad")
+
+
+def dev_grad_f32(ptr, n, sp: GradSpec, unit, step, replica, scale, offset=0, stream=0):
+    _check(dev().syn_dev_fill_grad_f32(ptr, n, offset, C.byref(sp), unit, step, replica, scale, stream),
+           "syn_dev_fill_grad_f32")
 
 
 def dev_normals(ptr, n, seed, tag, a=0, b=0, c=0, stream=0):

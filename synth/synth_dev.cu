@@ -25,6 +25,14 @@ __global__ void k_fill_grad(uint16_t *out, int64_t n, int64_t offset, syn_grad_s
         out[j] = syn_grad_bf16(&sp, unit, step, replica, (uint64_t)(offset + j), scale);
 }
 
+__global__ void k_fill_grad_f32(float *out, int64_t n, int64_t offset, syn_grad_spec sp,
+                                uint32_t unit, uint32_t step, uint32_t replica, float scale)
+{
+    int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t j = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n; j += stride)
+        out[j] = syn_grad_value(&sp, unit, step, replica, (uint64_t)(offset + j), scale);
+}
+
 __global__ void k_normals(float *out, int64_t n, uint32_t seed, uint32_t tag, uint32_t a, uint32_t b, uint32_t c)
 {
     int64_t stride = (int64_t)gridDim.x * blockDim.x;
@@ -60,6 +68,7 @@ typedef struct {
     const int64_t *seg_len;     /* host, per segment */
     const float *seg_scale;     /* host, per segment */
     float default_scale;
+    int32_t fp32_grads;         /* fill FP32 replicas (values before the BF16 rounding) */
 } syn_model_grads;
 
 int syn_dev_fill_master(float *out, int64_t n, int64_t offset, uint32_t seed, uint32_t unit, float scale,
@@ -75,6 +84,14 @@ int syn_dev_fill_grad(uint16_t *out, int64_t n, int64_t offset, const syn_grad_s
 {
     if (n <= 0) return 0;
     k_fill_grad<<<grid_for(n), kThreads, 0, s>>>(out, n, offset, *sp, unit, step, replica, scale);
+    return (int)cudaGetLastError();
+}
+
+int syn_dev_fill_grad_f32(float *out, int64_t n, int64_t offset, const syn_grad_spec *sp,
+                          uint32_t unit, uint32_t step, uint32_t replica, float scale, cudaStream_t s)
+{
+    if (n <= 0) return 0;
+    k_fill_grad_f32<<<grid_for(n), kThreads, 0, s>>>(out, n, offset, *sp, unit, step, replica, scale);
     return (int)cudaGetLastError();
 }
 
@@ -94,16 +111,17 @@ int syn_dev_grad_fn(void *user, int32_t layer, void *const *replicas, cudaStream
     if (!g || layer < 0 || layer >= g->n_units) return -1;
     uint32_t unit = g->unit_id_base + (uint32_t)layer;
     for (int32_t r = 0; r < g->n_replicas; ++r) {
-        uint16_t *dst = (uint16_t *)replicas[r];
-        if (g->seg_begin) {
-            for (int32_t k = g->seg_begin[layer]; k < g->seg_begin[layer + 1]; ++k) {
-                int rc = syn_dev_fill_grad(dst + g->seg_offset[k], g->seg_len[k], g->seg_offset[k], &g->spec,
-                                           unit, g->step, (uint32_t)r, g->seg_scale[k], s);
-                if (rc) return rc;
-            }
-        } else {
-            int rc = syn_dev_fill_grad(dst, g->unit_numel[layer], 0, &g->spec, unit, g->step, (uint32_t)r,
-                                       g->default_scale, s);
+        const int32_t nseg = g->seg_begin ? g->seg_begin[layer + 1] - g->seg_begin[layer] : 1;
+        for (int32_t q = 0; q < nseg; ++q) {
+            const int32_t k = g->seg_begin ? g->seg_begin[layer] + q : 0;
+            const int64_t off = g->seg_begin ? g->seg_offset[k] : 0;
+            const int64_t len = g->seg_begin ? g->seg_len[k] : g->unit_numel[layer];
+            const float scale = g->seg_begin ? g->seg_scale[k] : g->default_scale;
+            int rc = g->fp32_grads
+                         ? syn_dev_fill_grad_f32((float *)replicas[r] + off, len, off, &g->spec, unit, g->step,
+                                                 (uint32_t)r, scale, s)
+                         : syn_dev_fill_grad((uint16_t *)replicas[r] + off, len, off, &g->spec, unit, g->step,
+                                             (uint32_t)r, scale, s);
             if (rc) return rc;
         }
     }
@@ -117,7 +135,7 @@ typedef struct {
     int32_t n_replicas;
     int32_t n_pool;
     uint32_t step;
-    int32_t pad_;
+    int32_t fp32_grads;          /* replicas are FP32 (4 bytes per value) */
     const int64_t *unit_numel;   /* host array [n_units] */
     void *const *pool;           /* host array [n_pool * n_replicas] of device pointers */
 } syn_pool_grads;
@@ -127,7 +145,7 @@ int syn_dev_pool_grad_fn(void *user, int32_t layer, void *const *replicas, cudaS
     const syn_pool_grads *p = (const syn_pool_grads *)user;
     if (!p || layer < 0 || p->n_pool < 1) return -1;
     const int k = (int)(((uint32_t)layer + p->step) % (uint32_t)p->n_pool);
-    const size_t bytes = (size_t)p->unit_numel[layer] * 2;
+    const size_t bytes = (size_t)p->unit_numel[layer] * (p->fp32_grads ? 4 : 2);
     for (int32_t r = 0; r < p->n_replicas; ++r) {
         cudaError_t e = cudaMemcpyAsync(replicas[r], p->pool[k * p->n_replicas + r], bytes,
                                         cudaMemcpyDeviceToDevice, s);

@@ -51,3 +51,21 @@ void syn_host_gather_grad(uint16_t *out, const int64_t *idx, int64_t n, const sy
     for (int64_t j = 0; j < n; ++j)
         out[j] = syn_grad_bf16(&s, unit, step, replica, (uint64_t)idx[j], scale);
 }
+
+void syn_host_fill_grad_f32(float *out, int64_t n, int64_t offset, const syn_grad_spec *sp,
+                            uint32_t unit, uint32_t step, uint32_t replica, float scale)
+{
+    syn_grad_spec s = *sp;
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < n; ++j)
+        out[j] = syn_grad_value(&s, unit, step, replica, (uint64_t)(offset + j), scale);
+}
+
+void syn_host_gather_grad_f32(float *out, const int64_t *idx, int64_t n, const syn_grad_spec *sp,
+                              uint32_t unit, uint32_t step, uint32_t replica, float scale)
+{
+    syn_grad_spec s = *sp;
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < n; ++j)
+        out[j] = syn_grad_value(&s, unit, step, replica, (uint64_t)idx[j], scale);
+}

@@ -72,6 +72,7 @@ class Workload:
     zero_prob: float = 0.0
     streamed: bool = False
     master_scale: float = 0.02
+    fp32_grads: bool = False             # FP32 gradient replicas instead of BF16
     lr: float = 1e-5
     beta1: float = 0.9
     beta2: float = 0.999
@@ -134,6 +135,15 @@ def config5() -> Workload:
                     description="8 h=8192 layers (7,021,395,968 params), host-resident, "
                                 "2-unit HBM window, R=8, Student-t(3) gradients x 1e-3 with "
                                 "0.1% exact zeros")
+
+
+def config2_fp32() -> Workload:
+    w = config2()
+    w.name = "h2560_R4_clip_fp32grads"
+    w.fp32_grads = True
+    w.description = ("config 2 with FP32 gradient replicas (FP32 gradient accumulation): "
+                     "26 + 4R bytes per parameter")
+    return w
 
 
 ALL = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}

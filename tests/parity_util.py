@@ -60,26 +60,31 @@ def unit_grad_host(w, unit_index, step, replica, idx=None):
     u = w.units[unit_index]
     sp = synth.spec(w.seed, w.grad_kind, w.zero_prob)
     scales = w.tensor_scales(unit_index)
+    dt = np.float32 if w.fp32_grads else np.uint16
+    fill = synth.grad_f32 if w.fp32_grads else synth.grad
+    gather = synth.gather_grad_f32 if w.fp32_grads else synth.gather_grad
     if idx is None:
-        out = np.empty(u.numel, np.uint16)
+        out = np.empty(u.numel, dt)
         for (off, n), sc in zip(u.segments(), scales):
-            out[off:off + n] = synth.grad(n, sp, unit_index, step, replica, sc, offset=off)
+            out[off:off + n] = fill(n, sp, unit_index, step, replica, sc, offset=off)
         return out
     idx = np.asarray(idx, np.int64)
-    out = np.empty(idx.size, np.uint16)
+    out = np.empty(idx.size, dt)
     bounds = np.cumsum([0] + [n for _, n in u.tensors])
     for k, sc in enumerate(scales):
         sel = (idx >= bounds[k]) & (idx < bounds[k + 1])
         if sel.any():
-            out[sel] = synth.gather_grad(idx[sel], sp, unit_index, step, replica, sc)
+            out[sel] = gather(idx[sel], sp, unit_index, step, replica, sc)
     return out
 
 
 def unit_grad_dev(w, unit_index, step, replica, ptr, stream=0):
     u = w.units[unit_index]
     sp = synth.spec(w.seed, w.grad_kind, w.zero_prob)
+    size = 4 if w.fp32_grads else 2
+    fill = synth.dev_grad_f32 if w.fp32_grads else synth.dev_grad
     for (off, n), sc in zip(u.segments(), w.tensor_scales(unit_index)):
-        synth.dev_grad(ptr + 2 * off, n, sp, unit_index, step, replica, sc, offset=off, stream=stream)
+        fill(ptr + size * off, n, sp, unit_index, step, replica, sc, offset=off, stream=stream)
 
 
 def sample_indices(n, k, seed=1234, extra=()):

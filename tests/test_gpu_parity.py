@@ -35,6 +35,11 @@ def dev_u16(n):
     return torch.empty(max(n, 1) + 64, dtype=torch.int16, device="cuda")
 
 
+def dev_grad_buf(n, fp32=False):
+    """Device buffer for one gradient replica of n values (BF16 or FP32)."""
+    return torch.empty(max(n, 1) + 64, dtype=torch.float32 if fp32 else torch.int16, device="cuda")
+
+
 def to_np_u16(t, n):
     return t[:n].cpu().numpy().view(np.uint16)
 
@@ -58,11 +63,13 @@ def test_generator_device_matches_host(S):
 
 # ------------------------------------------------------ small, every element ----
 
-def run_small(S, sizes, R, clip, steps=4, seed=11, flags=0, bf16_external=False):
+def run_small(S, sizes, R, clip, steps=4, seed=11, flags=0, bf16_external=False, fp32=False):
     """Multi-layer state with the given layer sizes; `steps` steps of every
     layer on fresh seeded grads; full comparison with the oracle after each."""
     w = W.Workload("small", [W.Unit(f"l{i}", [("flat", n)]) for i, n in enumerate(sizes)],
-                   R=R, steps=steps, seed=seed, max_grad_norm=clip, lr=1e-3)
+                   R=R, steps=steps, seed=seed, max_grad_norm=clip, lr=1e-3, fp32_grads=fp32)
+    if fp32:
+        flags |= S.SLIDE_FLAG_FP32_GRADS
     hp_dev = S.hparams(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_grad_norm)
     hp_or = pu.hp_oracle(w)
     st = S.slide_state_create(sizes, R, flags=flags)
@@ -74,7 +81,7 @@ def run_small(S, sizes, R, clip, steps=4, seed=11, flags=0, bf16_external=False)
             S.slide_layer_set(st, li, master=th0, step=0)
             ref.append([th0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32),
                         np.zeros(n, np.uint16)])
-        grads = [dev_u16(max(sizes)) for _ in range(R)]
+        grads = [dev_grad_buf(max(sizes), fp32) for _ in range(R)]
         outs = [dev_u16(n) for n in sizes] if bf16_external else None
         for t in range(1, steps + 1):
             for li, n in enumerate(sizes):
@@ -153,6 +160,17 @@ def test_eps_regime_bit_exact(S, scale):
         assert all(r["not_bit_equal"] == 0 for r in rep), rep
     finally:
         S.slide_state_destroy(st)
+
+
+@pytest.mark.parametrize("R", [1, 3, 4, 8])
+@pytest.mark.parametrize("clip", [0.0, 1e-3])
+def test_small_parity_fp32_grads(S, R, clip):
+    """FP32 gradient replicas (26 + 4R bytes per parameter): same arithmetic
+    after the widening, so bit-exact without a clip."""
+    reps = run_small(S, [1, 9, 4096 + 3, (1 << 20) + 5], R, clip=clip, fp32=True)
+    if clip == 0.0:
+        for r in reps:
+            assert r["not_bit_equal"] == 0, r
 
 
 def test_external_bf16_out_and_empty_layer(S):
@@ -281,7 +299,7 @@ def run_full_size(S, w, n_samples=200_000):
     t0 = 0
     th_s = synth.gather_master(idx, w.seed)
     m_s, v_s = np.zeros(idx.size, np.float32), np.zeros(idx.size, np.float32)
-    st = S.slide_state_create([n], w.R)
+    st = S.slide_state_create([n], w.R, flags=S.SLIDE_FLAG_FP32_GRADS if w.fp32_grads else 0)
     try:
         th_d = S.slide_layer_ptrs(st, 0)[0]
         synth.dev_master(th_d, n, w.seed)
@@ -304,7 +322,7 @@ def run_full_size(S, w, n_samples=200_000):
             th_s, m_s, v_s = th[idx].copy(), m[idx].copy(), v[idx].copy()
             del th, m, v
             t0 = w.prewarm_steps
-        grads = [dev_u16(n) for _ in range(w.R)]
+        grads = [dev_grad_buf(n, w.fp32_grads) for _ in range(w.R)]
         hp = S.hparams(*w.hparams_tuple())
         for t in range(t0 + 1, t0 + w.steps + 1):
             for r in range(w.R):
@@ -328,7 +346,8 @@ def run_full_size(S, w, n_samples=200_000):
         S.slide_state_destroy(st)
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3])
+@pytest.mark.parametrize("cfg", [1, 2, 3, "2-fp32"])
 def test_full_size_workload_sampled(S, cfg):
-    rep = run_full_size(S, W.ALL[cfg]())
+    w = W.config2_fp32() if cfg == "2-fp32" else W.ALL[cfg]()
+    rep = run_full_size(S, w)
     print(rep)

@@ -51,7 +51,7 @@ class ModelGradsHolder:
         self.mg = synth.ModelGrads(synth.spec(w.seed, w.grad_kind, w.zero_prob), len(w.units), w.R, step, 0,
                                    C.cast(self.numel, C.c_void_p), C.cast(self.seg_begin, C.c_void_p),
                                    C.cast(self.seg_off, C.c_void_p), C.cast(self.seg_len, C.c_void_p),
-                                   C.cast(self.seg_scale, C.c_void_p), w.grad_scale)
+                                   C.cast(self.seg_scale, C.c_void_p), w.grad_scale, int(w.fp32_grads))
 
 
 def init_streamed(S, w, st):
@@ -77,17 +77,18 @@ def check_timeline(S, st, sizes):
     assert all(ends[l] >= ends[l + 1] - 1e-3 for l in range(len(units) - 1))
 
 
-def toy(R=3, clip=0.0, seed=5):
+def toy(R=3, clip=0.0, seed=5, fp32=False):
     sizes = [5000, 70001, (1 << 20) + 3, 0, 777, 123457]
     return W.Workload("toy", [W.Unit(f"u{i}", [("a", n // 2), ("b", n - n // 2)]) for i, n in enumerate(sizes)],
-                      R=R, steps=3, seed=seed, max_grad_norm=clip, lr=1e-3, streamed=True)
+                      R=R, steps=3, seed=seed, max_grad_norm=clip, lr=1e-3, streamed=True, fp32_grads=fp32)
 
 
-@pytest.mark.parametrize("clip,chunk", [(0.0, 64 << 10), (0.5, 256), (1e4, 1 << 20)])
-def test_streamed_toy_every_element(S, clip, chunk):
-    w = toy(clip=clip)
+@pytest.mark.parametrize("clip,chunk,fp32", [(0.0, 64 << 10, False), (0.5, 256, False), (1e4, 1 << 20, False),
+                                             (0.0, 64 << 10, True), (0.5, 4096, True)])
+def test_streamed_toy_every_element(S, clip, chunk, fp32):
+    w = toy(clip=clip, fp32=fp32)
     st = S.slide_state_create([u.numel for u in w.units], w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED,
-                              chunk_bytes=chunk)
+                              chunk_bytes=chunk, flags=S.SLIDE_FLAG_FP32_GRADS if fp32 else 0)
     try:
         init_streamed(S, w, st)
         ref = []
