@@ -274,6 +274,75 @@ def run_fp32_variant(args, S, torch, synth, peak):
             "step_roofline_frac": (b_upd + b_pre) / (ms / K * 1e-3) / 1e9 / peak}
 
 
+# ---------------------------------------------------- CPU-reduce route ----
+
+def host_replica_mean(reps_bf16):
+    """Mean of R BF16 replicas on the host: widen, FP32 sum in replica order,
+    divide by R (the reduction the CPU route performs)."""
+    import numpy as np
+    acc = (reps_bf16[0].astype(np.uint32) << 16).view(np.float32).copy()
+    for g in reps_bf16[1:]:
+        acc += (g.astype(np.uint32) << 16).view(np.float32)
+    acc /= np.float32(len(reps_bf16))
+    return acc
+
+
+def measure_cpu_reduce_route(S, torch, synth, n, R, seed=1, hp=None):
+    """The CPU-reduce route of the pages (every replica leaves the GPU and is
+    reduced on the host: R x 2n bytes device->host) against the GPU route
+    (the replicas are averaged inside the update kernel and never leave HBM).
+    The host mean returns to the GPU as one FP32 replica (4n bytes), so both
+    routes must produce bit-identical states; that is checked."""
+    import numpy as np
+    hp = hp or S.hparams(max_grad_norm=1.0)
+    sp = synth.spec(seed)
+    reps = [torch.empty(n + 64, dtype=torch.int16, device="cuda") for _ in range(R)]
+    for r in range(R):
+        synth.dev_grad(reps[r].data_ptr(), n, sp, 0, 1, r, 1e-3)
+    th0 = synth.master(n, seed)
+    gpu = S.slide_state_create([n], R)
+    cpu = S.slide_state_create([n], 1, flags=S.SLIDE_FLAG_FP32_GRADS)
+    host_reps = [torch.empty(n, dtype=torch.int16, pin_memory=True) for _ in range(R)]
+    mean_host = torch.empty(n, dtype=torch.float32, pin_memory=True)
+    mean_dev = torch.empty(n + 64, dtype=torch.float32, device="cuda")
+    try:
+        S.slide_layer_set(gpu, 0, master=th0, step=0)
+        S.slide_layer_set(cpu, 0, master=th0, step=0)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        S.slide_layer_step(gpu, 0, reps, hp)
+        torch.cuda.synchronize()
+        t_gpu = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        for r in range(R):
+            host_reps[r].copy_(reps[r][:n], non_blocking=True)
+        torch.cuda.synchronize()
+        t_d2h = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        mean = host_replica_mean([h.numpy().view(np.uint16) for h in host_reps])
+        t_reduce = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        mean_host.numpy()[:] = mean
+        mean_dev[:n].copy_(mean_host, non_blocking=True)
+        S.slide_layer_step(cpu, 0, [mean_dev], hp)
+        torch.cuda.synchronize()
+        t_back = time.perf_counter() - t0
+        a = [np.empty(n, np.float32) for _ in range(3)] + [np.empty(n, np.uint16)]
+        b = [np.empty(n, np.float32) for _ in range(3)] + [np.empty(n, np.uint16)]
+        S.slide_layer_get(gpu, 0, *a)
+        S.slide_layer_get(cpu, 0, *b)
+        same = all(np.array_equal(x.view(np.uint8), y.view(np.uint8)) for x, y in zip(a, b))
+    finally:
+        S.slide_state_destroy(gpu)
+        S.slide_state_destroy(cpu)
+    return {"params": n, "replicas": R, "identical_results": bool(same),
+            "gpu_route": {"s": t_gpu, "link_bytes": 0},
+            "cpu_route": {"s": t_d2h + t_reduce + t_back, "d2h_s": t_d2h, "host_reduce_s": t_reduce,
+                          "h2d_and_update_s": t_back, "link_bytes": R * 2 * n + 4 * n,
+                          "host_reduce": "numpy FP32 in replica order, one host thread"},
+            "amplification_d2h_bytes": f"{R} x 2n (every replica) instead of none"}
+
+
 # ----------------------------------------------------------- streamed ----
 
 def kernel_source_sha256():
@@ -373,6 +442,30 @@ def timeline_overlap(units, fwd_end):
             "units_ms": [{k: round(v, 3) for k, v in u.items()} for u in units]}
 
 
+def measure_delivery(S, torch, st, layer, n, R, reps=3):
+    """Delivery of one unit's BF16 copy from the pinned host mirror to R
+    consumer buffers: full (R copies over the host link) against sharded (one
+    copy's worth over the link, then an on-device all-gather)."""
+    dst = [torch.empty(n + 64, dtype=torch.int16, device="cuda") for _ in range(R)]
+    stream = torch.cuda.Stream()
+    out = {"params": n, "consumers": R}
+    for name, route in (("full", S.SLIDE_DELIVER_FULL), ("sharded", S.SLIDE_DELIVER_SHARDED)):
+        best = None
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(stream)
+            S.slide_deliver_bf16(st, layer, dst, route=route, stream=stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+        out[name] = {"ms": best, "host_link_bytes": (R if route == S.SLIDE_DELIVER_FULL else 1) * 2 * n,
+                     "device_bytes": 0 if route == S.SLIDE_DELIVER_FULL else 2 * (R - 1) * 2 * n}
+    del dst
+    return out
+
+
 def run_streamed(args, S, torch, synth):
     """Host-resident streamed step of a whole model: s/step against the
     host-link roofline measured in the same run.  The gradient callback stands
@@ -422,6 +515,7 @@ def run_streamed(args, S, torch, synth):
             times.append(time.perf_counter() - t0)
         units_tl, fwd_end = S.slide_streamed_timeline(st)
         overlap = timeline_overlap(units_tl, fwd_end)
+        delivery = measure_delivery(S, torch, st, 0, sizes[0], w.R)
         t0 = time.perf_counter()
         S.slide_model_step_streamed(st, fn_gen, mg, hp)
         gen_s = time.perf_counter() - t0
@@ -445,6 +539,7 @@ def run_streamed(args, S, torch, synth):
                              "from HBM into the window",
             "s_per_step_with_generator_callback": gen_s,
             "timeline_last_step": overlap,
+            "bf16_delivery": delivery,
             "timing": "host wall clock around each synchronous model step"}
 
 
@@ -601,8 +696,10 @@ def run_ours(args):
         S.slide_state_destroy(st)
 
     variant = None
+    cpu_route = None
     if not args.no_variants and world == 1:
         variant = run_fp32_variant(args, S, torch, synth, measured_peaks()[0])
+        cpu_route = measure_cpu_reduce_route(S, torch, synth, n, R)
     streamed = None
     if not args.no_streamed and world == 1:
         streamed = run_streamed(args, S, torch, synth)
@@ -666,6 +763,7 @@ def run_ours(args):
         "e2e": e2e,
         "cpu_baseline": cpu,
         "fp32_grad_variant": variant,
+        "cpu_reduce_route": cpu_route,
         "streamed": streamed,
     }
     print(json.dumps(line), flush=True)

@@ -245,6 +245,29 @@ SLIDE_API slide_status slide_adamw_step_noalloc(int64_t n, int32_t n_replicas, c
                                                 const slide_adam_hparams *hp, int64_t step,
                                                 slide_stream_t stream);
 
+enum {
+    SLIDE_DELIVER_FULL = 0,    /* every consumer receives the whole copy from the source */
+    SLIDE_DELIVER_SHARDED = 1  /* consumer r receives shard r from the source, then the shards
+                                  are gathered on the device (consumer to consumer) */
+};
+
+/* Delivery of a layer's BF16 compute copy to R consumer buffers on the GPU
+ * (the R ranks' copies of the next forward's weights, modelled as R device
+ * buffers).  Source: the state's BF16 copy, in HBM (HBM residency) or in the
+ * pinned host mirror (streamed residency).  With SLIDE_DELIVER_FULL each
+ * consumer gets a full copy from the source (R x 2n bytes leave the source);
+ * with SLIDE_DELIVER_SHARDED consumer r gets elements [r*s, (r+1)*s) (s = n/R
+ * rounded up to a multiple of 8, the last shard shorter) from the source, and
+ * then copies the other shards from their owners on the device (2n bytes leave
+ * the source, (R-1) x 2n move inside HBM).  "SlideDP: Scaling Host-Resident
+ * LLM Fine-Tuning Across Multiple GPUs", Core method: full delivery versus
+ * sharded delivery plus GPU all-gather.
+ *   dst: host array of n_consumers device pointers (16-byte aligned), each to
+ *   layer_numel[layer] BF16 values; n_consumers in [1, 8].  Stream-ordered on
+ *   `stream`; the source must not be updated until the delivery has run. */
+SLIDE_API slide_status slide_deliver_bf16(slide_state *st, int32_t layer, void *const *dst, int32_t n_consumers,
+                                          int32_t route, slide_stream_t stream);
+
 /* Timeline of the last slide_model_step_streamed, for tracing how the copies
  * and the updates overlap (host-streamed residency).  out receives, for each
  * unit l, 6 values in milliseconds from the start of that step:

@@ -37,6 +37,8 @@ SLIDE_FLAG_CHECK_FINITE = 1
 SLIDE_FLAG_TEST_PIPELINE_STALL = 2
 SLIDE_FLAG_FP32_GRADS = 4
 SLIDE_MAX_REPLICAS = 8
+SLIDE_DELIVER_FULL = 0
+SLIDE_DELIVER_SHARDED = 1
 
 
 class SlideError(RuntimeError):
@@ -87,6 +89,8 @@ def _load():
     L.slide_layer_last_clip_coef.restype = S
     L.slide_layer_status.argtypes = [P, C.c_int32]
     L.slide_layer_status.restype = S
+    L.slide_deliver_bf16.argtypes = [P, C.c_int32, C.POINTER(C.c_void_p), C.c_int32, C.c_int32, P]
+    L.slide_deliver_bf16.restype = S
     L.slide_streamed_timeline.argtypes = [P, C.POINTER(C.c_double), C.c_int64]
     L.slide_streamed_timeline.restype = S
     L.slide_trace_events.argtypes = [P, P, P, P]
@@ -293,3 +297,10 @@ def slide_streamed_timeline(st: SlideState):
     keys = ("h2d_begin", "master_landed", "h2d_end", "update_end", "d2h_begin", "d2h_end")
     units = [dict(zip(keys, buf[6 * l:6 * l + 6])) for l in range(L)]
     return units, buf[6 * L]
+
+
+def slide_deliver_bf16(st: SlideState, layer: int, dst, route=SLIDE_DELIVER_FULL, stream=None) -> None:
+    """Deliver a layer's BF16 copy to len(dst) consumer device buffers."""
+    ptrs = [_ptr(d) for d in dst]
+    arr = (C.c_void_p * max(1, len(ptrs)))(*ptrs)
+    _check(_lib().slide_deliver_bf16(C.c_void_p(st.handle), layer, arr, len(ptrs), route, _stream(stream)))

@@ -516,6 +516,61 @@ slide_status slide_trace_events(slide_state *st, void *ev_prepass_start, void *e
     return SLIDE_OK;
 }
 
+slide_status slide_deliver_bf16(slide_state *st, int32_t layer, void *const *dst, int32_t n_consumers,
+                                int32_t route, slide_stream_t stream)
+{
+    slide_status rc = check_layer(st, layer);
+    if (rc != SLIDE_OK)
+        return rc;
+    if (n_consumers < 1 || n_consumers > SLIDE_MAX_REPLICAS || !dst)
+        return fail(SLIDE_ERR_INVALID_ARG, "n_consumers must lie in [1, 8] with a dst array");
+    if (route != SLIDE_DELIVER_FULL && route != SLIDE_DELIVER_SHARDED)
+        return fail(SLIDE_ERR_INVALID_ARG, "unknown delivery route");
+    LayerState &L = st->layers[layer];
+    for (int r = 0; r < n_consumers; ++r)
+        if (L.n > 0 && (!dst[r] || !aligned16(dst[r])))
+            return fail(SLIDE_ERR_INVALID_ARG, "consumer pointer is NULL or not 16-byte aligned");
+    if (L.n == 0) {
+        clear_error();
+        return SLIDE_OK;
+    }
+    DeviceGuard guard(st->device);
+    if (!guard.ok)
+        return fail(SLIDE_ERR_CUDA, "cudaSetDevice failed");
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t n = (size_t)L.n;
+    cudaError_t e = cudaSuccess;
+    if (route == SLIDE_DELIVER_FULL || n_consumers == 1) {
+        for (int r = 0; r < n_consumers && e == cudaSuccess; ++r)
+            e = cudaMemcpyAsync(dst[r], L.w, n * 2, cudaMemcpyDefault, s);
+    } else {
+        // shard size: n / R rounded up to 8 elements (16 bytes) so every shard starts aligned
+        const size_t shard = ((n + n_consumers - 1) / n_consumers + 7) & ~(size_t)7;
+        for (int r = 0; r < n_consumers && e == cudaSuccess; ++r) {
+            const size_t off = (size_t)r * shard;
+            if (off >= n)
+                break;
+            const size_t len = n - off < shard ? n - off : shard;
+            e = cudaMemcpyAsync((uint16_t *)dst[r] + off, L.w + off, len * 2, cudaMemcpyDefault, s);
+        }
+        // all-gather on the device: consumer q takes shard r from its owner r
+        for (int r = 0; r < n_consumers && e == cudaSuccess; ++r) {
+            const size_t off = (size_t)r * shard;
+            if (off >= n)
+                break;
+            const size_t len = n - off < shard ? n - off : shard;
+            for (int q = 0; q < n_consumers && e == cudaSuccess; ++q)
+                if (q != r)
+                    e = cudaMemcpyAsync((uint16_t *)dst[q] + off, (const uint16_t *)dst[r] + off, len * 2,
+                                        cudaMemcpyDeviceToDevice, s);
+        }
+    }
+    if (e != cudaSuccess)
+        return fail_cuda(e, "slide_deliver_bf16 copies");
+    clear_error();
+    return SLIDE_OK;
+}
+
 slide_status slide_streamed_timeline(slide_state *st, double *out, int64_t cap)
 {
     if (!st || !out)

@@ -7,9 +7,10 @@
 //    memory, a small reusable BF16 layer window on the GPU, layers swapped in
 //    forward order for the forward pass and in reverse order for the backward
 //    pass) and Core method / Method steps (one authoritative host copy of the
-//    FP32 master and Adam moments per layer; per-chunk pipelining of copies and
-//    updates; the version gate: the next delivery of a layer waits for its
-//    update; slots are reused only after their copies complete).
+//    FP32 master and Adam moments per layer; per-chunk pipelining: a chunk's
+//    update is released as soon as that chunk has arrived; the version gate:
+//    the next delivery of a layer waits for its update; slots are reused only
+//    after their copies complete).
 //  - "An Efficient Heterogeneous Co-Design for Fine-Tuning on a Single GPU"
 //    (SlideFormer), sections 2.1-2.2: while layer i is processed the next one
 //    is prefetched and the previous one's update proceeds; a pre-allocated,
@@ -27,22 +28,25 @@
 //   device -> host: 12 B (master, m, v) + 2 B (new BF16 copy)
 // and the R gradient replicas never leave HBM.
 //
-// Schedule of one step (all enqueued up front; the host then waits once):
-//  forward sweep on the H2D stream: BF16 copy of unit l -> slot l%2;
+// A unit's arrays are split into chunks of chunk_bytes of FP32 (the BF16
+// copy and the replicas use the same element ranges).  Schedule of one step,
+// all enqueued up front, then one bounded host wait per stream:
+//  forward sweep (H2D stream): the BF16 copy of unit l -> slot l%2, in order;
 //  reverse sweep, l = L-1 .. 0, slot s = l%2:
-//    H2D stream:     master/m/v of l -> slot s, chunk by chunk; chunk k of each
-//                    array first waits for the D2H of the same chunk of the
-//                    unit that last used slot s (l+2), so the copy-in of l
-//                    trails the copy-out of l+2 by one chunk;
-//    compute stream: once the master of l has landed, grad_fn(l) fills the R
-//                    replicas (while m and v still arrive); then, after the
-//                    rest of l's H2D and the D2H of the BF16 copy of l+2, the
-//                    clip pre-pass and the fused kernel update slot s in place;
-//    D2H stream:     wait for the kernel; BF16 copy, then master/m/v of l back
-//                    to the host, chunk by chunk, each chunk recording the
-//                    event the next copy-in to the same bytes waits for.
-//  While the kernel updates l, the H2D engine is filling the other slot with
-//  l-1 and the D2H engine is draining l+1 out of it.
+//    H2D stream:     the master of l, then its m and v chunk by chunk; every
+//                    chunk first waits for the write-back of the same bytes by
+//                    the unit that used slot s before (l+2), so a slot is
+//                    handed over chunk by chunk;
+//    compute stream: once the master has landed, grad_fn(l) fills the R
+//                    replicas (backward's stand-in) and the clip pre-pass runs
+//                    over the whole unit; then the fused update of chunk k is
+//                    launched as soon as m_k and v_k have landed and the BF16
+//                    chunk of l+2 has been written back;
+//    D2H stream:     the write-back of chunk k (BF16 copy, master, m, v)
+//                    follows its update, each piece recording the event that
+//                    the next copy-in to those bytes waits for.
+//  So the write-back of l starts while m and v of l are still arriving, the
+//  H2D engine fills the other slot with l-1 and the D2H engine drains l+1.
 #include <cuda_runtime.h>
 
 #include <chrono>
@@ -58,16 +62,17 @@ namespace slide {
 namespace {
 
 constexpr int kSlots = 2;
-constexpr int kRegions = 3;  // master, m, v (the arrays the next copy-in overwrites)
+enum Region { kTheta = 0, kM = 1, kV = 2, kW = 3, kRegions = 4 };
 
 struct Slot {
-    float *arr[kRegions] = {nullptr, nullptr, nullptr};  // master, m, v
+    float *arr[3] = {nullptr, nullptr, nullptr};  // master, m, v
     uint16_t *w = nullptr;
     void *g[kMaxReplicas] = {};
     ClipScratch scratch{};
-    // chunk k of region r freed by the D2H of the unit that used this slot last
+    // chunk k of region r has been written back by the unit that used this slot last
     std::vector<cudaEvent_t> freed[kRegions];
-    cudaEvent_t w_freed = nullptr;  // D2H of the BF16 copy done
+    std::vector<cudaEvent_t> mv_landed;  // chunk k of m and v has arrived
+    std::vector<cudaEvent_t> upd_done;   // chunk k has been updated
 };
 
 size_t grad_bytes(const slide_config &cfg) { return (cfg.flags & SLIDE_FLAG_FP32_GRADS) ? 4 : 2; }
@@ -78,25 +83,34 @@ size_t slot_bytes(int64_t maxn, int R, size_t gsize)
            align_up((size_t)maxn * gsize) * (size_t)R + scratch_bytes();
 }
 
+// Element range of chunk k of a unit of n parameters.
+struct Chunk {
+    int64_t off, len;
+};
+
 }  // namespace
 
 struct StreamEngine {
     void *window = nullptr;
     size_t window_bytes = 0;
     Slot slots[kSlots];
-    int64_t chunk_bytes = 0;
-    int chunks_per_region = 0;
+    int64_t chunk_elems = 0;  // parameters per chunk
+    int max_chunks = 0;
+    size_t gsize = 2;         // bytes per gradient value
     cudaStream_t s_h2d = nullptr, s_comp = nullptr, s_d2h = nullptr;
-    std::vector<cudaEvent_t> theta_done;  // per unit: the master has landed in its slot
-    std::vector<cudaEvent_t> h2d_done;    // per unit: master, m and v have landed
-    std::vector<cudaEvent_t> kern_done;   // per unit
-    cudaEvent_t fwd_done = nullptr;
+    // per unit, timing events (also the timeline of the last step)
+    std::vector<cudaEvent_t> h2d_begin, theta_done, h2d_done, kern_done, d2h_begin, d2h_end;
+    std::vector<char> recorded;  // unit reached its write-back in the last step
+    cudaEvent_t step_start = nullptr, fwd_done = nullptr;
     cudaEvent_t sweep_done[3] = {nullptr, nullptr, nullptr};  // end of the H2D, compute, D2H streams
-    // timeline of the last step (timing events): start, and per unit the
-    // begin of its copy-in and the begin/end of its write-back
-    cudaEvent_t step_start = nullptr;
-    std::vector<cudaEvent_t> h2d_begin, d2h_begin, d2h_end;
-    std::vector<char> recorded;  // unit reached write-back in the last step
+
+    Chunk chunk(int64_t n, int k) const
+    {
+        const int64_t off = (int64_t)k * chunk_elems;
+        const int64_t len = n - off < chunk_elems ? n - off : chunk_elems;
+        return {off, len};
+    }
+    int n_chunks(int64_t n) const { return (int)((n + chunk_elems - 1) / chunk_elems); }
 };
 
 size_t engine_device_bytes(const slide_config &cfg, int64_t max_numel)
@@ -106,32 +120,21 @@ size_t engine_device_bytes(const slide_config &cfg, int64_t max_numel)
 
 static void destroy_engine_objects(StreamEngine *E)
 {
-    for (Slot &s : E->slots) {
-        for (auto &v : s.freed)
-            for (cudaEvent_t ev : v)
-                if (ev)
-                    cudaEventDestroy(ev);
-        if (s.w_freed)
-            cudaEventDestroy(s.w_freed);
-    }
-    for (cudaEvent_t ev : E->h2d_done)
-        if (ev)
-            cudaEventDestroy(ev);
-    for (cudaEvent_t ev : E->theta_done)
-        if (ev)
-            cudaEventDestroy(ev);
-    for (cudaEvent_t ev : E->kern_done)
-        if (ev)
-            cudaEventDestroy(ev);
-    if (E->fwd_done)
-        cudaEventDestroy(E->fwd_done);
-    if (E->step_start)
-        cudaEventDestroy(E->step_start);
-    for (auto *vec : {&E->h2d_begin, &E->d2h_begin, &E->d2h_end})
-        for (cudaEvent_t ev : *vec)
+    auto kill = [](std::vector<cudaEvent_t> &v) {
+        for (cudaEvent_t ev : v)
             if (ev)
                 cudaEventDestroy(ev);
-    for (cudaEvent_t ev : E->sweep_done)
+        v.clear();
+    };
+    for (Slot &s : E->slots) {
+        for (auto &v : s.freed)
+            kill(v);
+        kill(s.mv_landed);
+        kill(s.upd_done);
+    }
+    for (auto *v : {&E->h2d_begin, &E->theta_done, &E->h2d_done, &E->kern_done, &E->d2h_begin, &E->d2h_end})
+        kill(*v);
+    for (cudaEvent_t ev : {E->step_start, E->fwd_done, E->sweep_done[0], E->sweep_done[1], E->sweep_done[2]})
         if (ev)
             cudaEventDestroy(ev);
     for (cudaStream_t s : {E->s_h2d, E->s_comp, E->s_d2h})
@@ -150,22 +153,23 @@ slide_status engine_create(slide_state *st)
     for (int64_t n : st->numel)
         maxn = n > maxn ? n : maxn;
     const int R = st->cfg.n_replicas;
-    E->chunk_bytes = st->cfg.chunk_bytes;
-    E->chunks_per_region = (int)((maxn * 4 + E->chunk_bytes - 1) / E->chunk_bytes);
+    E->gsize = grad_bytes(st->cfg);
+    E->chunk_elems = st->cfg.chunk_bytes / 4;  // chunk_bytes is a positive multiple of 256
+    E->max_chunks = E->n_chunks(maxn);
     E->window_bytes = engine_device_bytes(st->cfg, maxn);
     cudaError_t e = cudaMalloc(&E->window, E->window_bytes);
     if (e != cudaSuccess) {
         cudaGetLastError();
         E->window = nullptr;
+        const size_t want = E->window_bytes;
         destroy_engine_objects(E);
         delete E;
-        return fail(SLIDE_ERR_OOM_DEVICE, "cudaMalloc of the HBM window (" + std::to_string(E->window_bytes) +
-                                              " bytes) failed");
+        return fail(SLIDE_ERR_OOM_DEVICE, "cudaMalloc of the HBM window (" + std::to_string(want) + " bytes) failed");
     }
     e = cudaMemset(E->window, 0, E->window_bytes);
     char *p = (char *)E->window;
     for (Slot &s : E->slots) {
-        for (int r = 0; r < kRegions; ++r) {
+        for (int r = 0; r < 3; ++r) {
             s.arr[r] = (float *)p;
             p += align_up((size_t)maxn * 4);
         }
@@ -173,47 +177,35 @@ slide_status engine_create(slide_state *st)
         p += align_up((size_t)maxn * 2);
         for (int r = 0; r < R; ++r) {
             s.g[r] = p;
-            p += align_up((size_t)maxn * grad_bytes(st->cfg));
+            p += align_up((size_t)maxn * E->gsize);
         }
         s.scratch.partials = (double *)p;
         s.scratch.coef = (float *)(p + align_up(sizeof(double) * kMaxPartials));
         s.scratch.status = (unsigned *)(s.scratch.coef + 1);
         p += scratch_bytes();
-        for (int r = 0; r < kRegions && e == cudaSuccess; ++r) {
-            s.freed[r].assign(E->chunks_per_region, nullptr);
-            for (auto &ev : s.freed[r])
+        auto make = [&](std::vector<cudaEvent_t> &v) {
+            v.assign(E->max_chunks, nullptr);
+            for (auto &ev : v)
                 if (e == cudaSuccess)
                     e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
-        }
-        if (e == cudaSuccess)
-            e = cudaEventCreateWithFlags(&s.w_freed, cudaEventDisableTiming);
+        };
+        for (auto &v : s.freed)
+            make(v);
+        make(s.mv_landed);
+        make(s.upd_done);
     }
     const size_t L = st->layers.size();
-    E->h2d_done.assign(L, nullptr);
-    E->theta_done.assign(L, nullptr);
-    E->kern_done.assign(L, nullptr);
-    E->h2d_begin.assign(L, nullptr);
-    E->d2h_begin.assign(L, nullptr);
-    E->d2h_end.assign(L, nullptr);
-    E->recorded.assign(L, 0);
-    // the events of the timeline keep timing; the others are sync-only
-    for (size_t l = 0; l < L && e == cudaSuccess; ++l) {
-        e = cudaEventCreate(&E->h2d_done[l]);
-        if (e == cudaSuccess)
-            e = cudaEventCreate(&E->theta_done[l]);
-        if (e == cudaSuccess)
-            e = cudaEventCreate(&E->kern_done[l]);
-        if (e == cudaSuccess)
-            e = cudaEventCreate(&E->h2d_begin[l]);
-        if (e == cudaSuccess)
-            e = cudaEventCreate(&E->d2h_begin[l]);
-        if (e == cudaSuccess)
-            e = cudaEventCreate(&E->d2h_end[l]);
+    for (auto *v : {&E->h2d_begin, &E->theta_done, &E->h2d_done, &E->kern_done, &E->d2h_begin, &E->d2h_end}) {
+        v->assign(L, nullptr);
+        for (auto &ev : *v)
+            if (e == cudaSuccess)
+                e = cudaEventCreate(&ev);
     }
-    if (e == cudaSuccess)
-        e = cudaEventCreate(&E->fwd_done);
+    E->recorded.assign(L, 0);
     if (e == cudaSuccess)
         e = cudaEventCreate(&E->step_start);
+    if (e == cudaSuccess)
+        e = cudaEventCreate(&E->fwd_done);
     for (int k = 0; k < 3 && e == cudaSuccess; ++k)
         e = cudaEventCreateWithFlags(&E->sweep_done[k], cudaEventDisableTiming);
     if (e == cudaSuccess)
@@ -266,34 +258,6 @@ static slide_status wait_event(cudaEvent_t ev, uint32_t timeout_ms, const char *
     }
 }
 
-// Copy `bytes` between host and window in chunks of the engine's chunk size.
-// Copy-in (dir = H2D): chunk k of region `region` first waits for that
-// chunk's freed event.  Copy-out (D2H): chunk k records the freed event.
-static cudaError_t copy_region(StreamEngine *E, Slot &slot, int region, void *dst, const void *src,
-                               size_t bytes, cudaMemcpyKind dir, cudaStream_t s)
-{
-    const size_t C = (size_t)E->chunk_bytes;
-    int k = 0;
-    for (size_t off = 0; off < bytes; off += C, ++k) {
-        const size_t len = bytes - off < C ? bytes - off : C;
-        cudaError_t e;
-        if (dir == cudaMemcpyHostToDevice) {
-            e = cudaStreamWaitEvent(s, slot.freed[region][k], 0);
-            if (e != cudaSuccess)
-                return e;
-        }
-        e = cudaMemcpyAsync((char *)dst + off, (const char *)src + off, len, dir, s);
-        if (e != cudaSuccess)
-            return e;
-        if (dir == cudaMemcpyDeviceToHost) {
-            e = cudaEventRecord(slot.freed[region][k], s);
-            if (e != cudaSuccess)
-                return e;
-        }
-    }
-    return cudaSuccess;
-}
-
 slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const slide_adam_hparams &hp)
 {
     StreamEngine *E = st->engine;
@@ -303,6 +267,8 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
     const AdamScalars sc = adam_scalars_for(hp, t);
     const bool clip = hp.max_grad_norm > 0.0f;
     const bool check = (st->cfg.flags & SLIDE_FLAG_CHECK_FINITE) != 0;
+    const bool stall = (st->cfg.flags & SLIDE_FLAG_TEST_PIPELINE_STALL) != 0;
+    const bool f32g = (st->cfg.flags & SLIDE_FLAG_FP32_GRADS) != 0;
     cudaError_t e = cudaSuccess;
     slide_status rc = SLIDE_OK;
     int done_units = 0;  // units whose update and write-back were enqueued (from L-1 down)
@@ -310,28 +276,49 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
     for (int l = 0; l < L; ++l)
         E->recorded[l] = 0;
     e = cudaEventRecord(E->step_start, E->s_h2d);
+
     // forward sweep: deliver the BF16 copy of every unit, in order
     for (int l = 0; l < L && e == cudaSuccess; ++l) {
         Slot &s = E->slots[l % kSlots];
         const LayerState &U = st->layers[l];
-        if (U.n > 0) {
-            e = cudaStreamWaitEvent(E->s_h2d, s.w_freed, 0);
+        for (int k = 0; k < E->n_chunks(U.n) && e == cudaSuccess; ++k) {
+            const Chunk c = E->chunk(U.n, k);
+            e = cudaStreamWaitEvent(E->s_h2d, s.freed[kW][k], 0);
             if (e == cudaSuccess)
-                e = cudaMemcpyAsync(s.w, U.w, (size_t)U.n * 2, cudaMemcpyHostToDevice, E->s_h2d);
+                e = cudaMemcpyAsync(s.w + c.off, U.w + c.off, (size_t)c.len * 2, cudaMemcpyHostToDevice, E->s_h2d);
         }
     }
     if (e == cudaSuccess)
         e = cudaEventRecord(E->fwd_done, E->s_h2d);
 
+    // copy-in of master, m, v of unit l (H2D stream)
     auto copy_in = [&](int l) -> cudaError_t {
         Slot &s = E->slots[l % kSlots];
         const LayerState &U = st->layers[l];
-        const float *src[kRegions] = {U.theta, U.m, U.v};
+        const int K = E->n_chunks(U.n);
         cudaError_t err = cudaEventRecord(E->h2d_begin[l], E->s_h2d);
-        for (int r = 0; r < kRegions && err == cudaSuccess; ++r) {
-            err = copy_region(E, s, r, s.arr[r], src[r], (size_t)U.n * 4, cudaMemcpyHostToDevice, E->s_h2d);
-            if (r == 0 && err == cudaSuccess)
-                err = cudaEventRecord(E->theta_done[l], E->s_h2d);
+        for (int k = 0; k < K && err == cudaSuccess; ++k) {
+            const Chunk c = E->chunk(U.n, k);
+            err = cudaStreamWaitEvent(E->s_h2d, s.freed[kTheta][k], 0);
+            if (err == cudaSuccess)
+                err = cudaMemcpyAsync(s.arr[0] + c.off, U.theta + c.off, (size_t)c.len * 4,
+                                      cudaMemcpyHostToDevice, E->s_h2d);
+        }
+        if (err == cudaSuccess)
+            err = cudaEventRecord(E->theta_done[l], E->s_h2d);
+        for (int k = 0; k < K && err == cudaSuccess; ++k) {
+            const Chunk c = E->chunk(U.n, k);
+            err = cudaStreamWaitEvent(E->s_h2d, s.freed[kM][k], 0);
+            if (err == cudaSuccess)
+                err = cudaMemcpyAsync(s.arr[1] + c.off, U.m + c.off, (size_t)c.len * 4, cudaMemcpyHostToDevice,
+                                      E->s_h2d);
+            if (err == cudaSuccess)
+                err = cudaStreamWaitEvent(E->s_h2d, s.freed[kV][k], 0);
+            if (err == cudaSuccess)
+                err = cudaMemcpyAsync(s.arr[2] + c.off, U.v + c.off, (size_t)c.len * 4, cudaMemcpyHostToDevice,
+                                      E->s_h2d);
+            if (err == cudaSuccess)
+                err = cudaEventRecord(s.mv_landed[k], E->s_h2d);
         }
         if (err == cudaSuccess)
             err = cudaEventRecord(E->h2d_done[l], E->s_h2d);
@@ -344,15 +331,15 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
     for (int l = L - 1; l >= 0 && e == cudaSuccess && rc == SLIDE_OK; --l) {
         Slot &s = E->slots[l % kSlots];
         LayerState &U = st->layers[l];
+        const int K = E->n_chunks(U.n);
         // prefetch the next unit of the sweep into the other slot
         if (l > 0) {
             e = copy_in(l - 1);
             if (e != cudaSuccess)
                 break;
         }
-        // gradients of l on the compute stream as soon as its master has landed
-        // (m and v keep arriving meanwhile), then the update once all of the
-        // unit is in and the slot's BF16 buffer has been written back
+        // gradients of l as soon as its master has landed, then the clip
+        // pre-pass over the whole unit, then chunk by chunk the update
         e = cudaStreamWaitEvent(E->s_comp, E->theta_done[l], 0);
         if (e != cudaSuccess)
             break;
@@ -368,43 +355,59 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
                 break;
             }
         }
-        e = cudaStreamWaitEvent(E->s_comp, E->h2d_done[l], 0);
-        if (e == cudaSuccess)
-            e = cudaStreamWaitEvent(E->s_comp, s.w_freed, 0);
-        if (e != cudaSuccess)
-            break;
-        if (U.n > 0) {
+        int n_partials = 0;
+        if (clip && U.n > 0) {
             ReplicaPtrs g{};
             for (int r = 0; r < R; ++r)
                 g.p[r] = s.g[r];
-            int n_partials = 0;
-            const bool f32g = (st->cfg.flags & SLIDE_FLAG_FP32_GRADS) != 0;
-            if (clip) {
-                e = launch_grad_sqnorm(g, R, U.n, s.scratch, &n_partials, st->device, E->s_comp, f32g);
-                if (e != cudaSuccess)
-                    break;
-            }
-            e = launch_grad_reduce_adamw_cast(g, R, U.n, s.arr[0], s.arr[1], s.arr[2], s.w, sc, &s.scratch,
-                                              n_partials, clip ? hp.max_grad_norm : 0.0f, check, st->device,
-                                              E->s_comp, (st->cfg.flags & SLIDE_FLAG_TEST_PIPELINE_STALL) != 0,
-                                              f32g);
+            e = launch_grad_sqnorm(g, R, U.n, s.scratch, &n_partials, st->device, E->s_comp, f32g);
             if (e != cudaSuccess)
                 break;
         }
-        e = cudaEventRecord(E->kern_done[l], E->s_comp);
+        for (int k = 0; k < K && e == cudaSuccess; ++k) {
+            const Chunk c = E->chunk(U.n, k);
+            e = cudaStreamWaitEvent(E->s_comp, s.mv_landed[k], 0);
+            if (e == cudaSuccess)
+                e = cudaStreamWaitEvent(E->s_comp, s.freed[kW][k], 0);
+            if (e != cudaSuccess)
+                break;
+            ReplicaPtrs gk{};
+            for (int r = 0; r < R; ++r)
+                gk.p[r] = (const char *)s.g[r] + (size_t)c.off * E->gsize;
+            e = launch_grad_reduce_adamw_cast(gk, R, c.len, s.arr[0] + c.off, s.arr[1] + c.off, s.arr[2] + c.off,
+                                              s.w + c.off, sc, &s.scratch, n_partials,
+                                              clip ? hp.max_grad_norm : 0.0f, check, st->device, E->s_comp, stall,
+                                              f32g);
+            if (e == cudaSuccess)
+                e = cudaEventRecord(s.upd_done[k], E->s_comp);
+        }
+        if (e == cudaSuccess)
+            e = cudaEventRecord(E->kern_done[l], E->s_comp);
         if (e != cudaSuccess)
             break;
-        // write l back: the BF16 copy first (frees the slot for the next kernel), then master/m/v
-        e = cudaStreamWaitEvent(E->s_d2h, E->kern_done[l], 0);
-        if (e == cudaSuccess)
-            e = cudaEventRecord(E->d2h_begin[l], E->s_d2h);
-        if (e == cudaSuccess && U.n > 0)
-            e = cudaMemcpyAsync(U.w, s.w, (size_t)U.n * 2, cudaMemcpyDeviceToHost, E->s_d2h);
-        if (e == cudaSuccess)
-            e = cudaEventRecord(s.w_freed, E->s_d2h);
-        float *dst[kRegions] = {U.theta, U.m, U.v};
-        for (int r = 0; r < kRegions && e == cudaSuccess; ++r)
-            e = copy_region(E, s, r, dst[r], s.arr[r], (size_t)U.n * 4, cudaMemcpyDeviceToHost, E->s_d2h);
+        // write-back of l, chunk by chunk behind its update
+        float *dst[3] = {U.theta, U.m, U.v};
+        for (int k = 0; k < K && e == cudaSuccess; ++k) {
+            const Chunk c = E->chunk(U.n, k);
+            e = cudaStreamWaitEvent(E->s_d2h, s.upd_done[k], 0);
+            if (e == cudaSuccess && k == 0)
+                e = cudaEventRecord(E->d2h_begin[l], E->s_d2h);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(U.w + c.off, s.w + c.off, (size_t)c.len * 2, cudaMemcpyDeviceToHost, E->s_d2h);
+            if (e == cudaSuccess)
+                e = cudaEventRecord(s.freed[kW][k], E->s_d2h);
+            for (int r = 0; r < 3 && e == cudaSuccess; ++r) {
+                e = cudaMemcpyAsync(dst[r] + c.off, s.arr[r] + c.off, (size_t)c.len * 4, cudaMemcpyDeviceToHost,
+                                    E->s_d2h);
+                if (e == cudaSuccess)
+                    e = cudaEventRecord(s.freed[r][k], E->s_d2h);
+            }
+        }
+        if (e == cudaSuccess && K == 0) {
+            e = cudaStreamWaitEvent(E->s_d2h, E->kern_done[l], 0);
+            if (e == cudaSuccess)
+                e = cudaEventRecord(E->d2h_begin[l], E->s_d2h);
+        }
         if (e == cudaSuccess)
             e = cudaEventRecord(E->d2h_end[l], E->s_d2h);
         if (e == cudaSuccess) {
@@ -423,9 +426,6 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
         wrc = e2 == cudaSuccess ? wait_event(E->sweep_done[k], st->cfg.timeout_ms, "streamed step")
                                 : fail_cuda(e2, "streamed step: record");
     }
-    if (rc == SLIDE_OK && wrc != SLIDE_OK)
-        rc = wrc;
-
     unsigned word = 0;
     if (wrc == SLIDE_OK) {
         for (int k = 0; k < kSlots; ++k) {
@@ -437,6 +437,9 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
         if ((word & 2u) && rc == SLIDE_OK)
             rc = fail(SLIDE_ERR_TIMEOUT, "a pipeline wait inside the update kernel reached its limit");
     }
+    if (rc == SLIDE_OK && wrc != SLIDE_OK)
+        rc = wrc;
+
     if (rc == SLIDE_OK) {
         for (LayerState &U : st->layers)
             U.t = t;
@@ -456,9 +459,9 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
 }
 
 // Timeline of the last step: per unit, milliseconds from the step's start to
-// [copy-in begin, master landed, copy-in end, update end, write-back begin,
-// write-back end]; then the end of the forward sweep.  NaN where a unit did
-// not get that far.
+// [copy-in begin, master landed, copy-in end, last chunk updated, write-back
+// of the first chunk may begin, write-back end]; then the end of the forward
+// sweep.  NaN where a unit did not get that far.
 slide_status engine_timeline(slide_state *st, double *out, int64_t cap)
 {
     StreamEngine *E = st->engine;
@@ -485,7 +488,7 @@ slide_status engine_timeline(slide_state *st, double *out, int64_t cap)
         o[5] = since(E->d2h_end[l]);
     }
     out[6 * L] = since(E->fwd_done);
-    cudaGetLastError();  // a NaN entry leaves a sticky-free "not ready" error behind
+    cudaGetLastError();
     return SLIDE_OK;
 }
 

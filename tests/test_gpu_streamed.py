@@ -63,18 +63,22 @@ def init_streamed(S, w, st):
 
 
 def check_timeline(S, st, sizes):
-    """The engine's per-unit events of the last step are in causal order:
-    copy-in, master landed, copy-in done, update, write-back; the write-back of
-    a unit starts after its update; units are written back in reverse order."""
+    """The engine's per-unit events of the last step respect causality: the
+    master lands after its copy-in began and before the copy-in ends; the
+    updates end after the copy-in ends; the write-back starts after the master
+    landed (the first chunk's update needs it) and ends after the last update;
+    units are written back in reverse order."""
     units, fwd_end = S.slide_streamed_timeline(st)
     assert np.isfinite(fwd_end) and fwd_end >= 0
-    order = ["h2d_begin", "master_landed", "h2d_end", "update_end", "d2h_begin", "d2h_end"]
+    eps = 1e-3
     for u in units:
-        vals = [u[k] for k in order]
-        assert all(np.isfinite(vals)), u
-        assert all(a <= b + 1e-3 for a, b in zip(vals, vals[1:])), u
+        assert all(np.isfinite(list(u.values()))), u
+        assert u["h2d_begin"] <= u["master_landed"] + eps <= u["h2d_end"] + 2 * eps, u
+        assert u["h2d_end"] <= u["update_end"] + eps, u
+        assert u["master_landed"] <= u["d2h_begin"] + eps, u
+        assert u["update_end"] <= u["d2h_end"] + eps and u["d2h_begin"] <= u["d2h_end"] + eps, u
     ends = [u["d2h_end"] for u in units]
-    assert all(ends[l] >= ends[l + 1] - 1e-3 for l in range(len(units) - 1))
+    assert all(ends[l] >= ends[l + 1] - eps for l in range(len(units) - 1))
 
 
 def toy(R=3, clip=0.0, seed=5, fp32=False):
