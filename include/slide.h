@@ -122,9 +122,10 @@ typedef struct {
 typedef struct slide_state slide_state; /* opaque; owns all of its memory */
 
 /* Gradient callback of the streamed step (stands in for a layer's backward):
- * fill the R BF16 replica buffers replica_dev_ptrs[0..R-1] of unit `layer`
- * (device pointers into the window, each layer_numel[layer] elements, owned by
- * the state) with work enqueued on `stream`.  replica_dev_ptrs[R] points to
+ * fill the R replica buffers replica_dev_ptrs[0..R-1] of unit `layer` (device
+ * pointers into the window, each layer_numel[layer] BF16 values, or FP32 values
+ * with SLIDE_FLAG_FP32_GRADS; owned by the state) with work enqueued on
+ * `stream`.  replica_dev_ptrs[R] points to
  * the unit's FP32 master weights in the window, the version being updated
  * (read-only), as a backward pass would read them.  Return 0 on success; any
  * other value aborts the sweep. */
@@ -150,7 +151,8 @@ SLIDE_API slide_status slide_state_bytes(const slide_config *cfg, int64_t *devic
  * clip pre-pass (if max_grad_norm > 0) and the fused kernel
  * grad_reduce_adamw_cast for step t = t_layer + 1, then set t_layer = t.
  *   grad_replicas: host array of R device pointers, each to layer_numel[layer]
- *     BF16 values, 16-byte aligned; caller-owned, read-only, and must stay
+ *     BF16 values (FP32 values with SLIDE_FLAG_FP32_GRADS), 16-byte aligned;
+ *     caller-owned, read-only, and must stay
  *     valid until the enqueued work has run.
  *   bf16_out: device pointer receiving the BF16 copy, or NULL for the state's
  *     own copy (slide_layer_ptrs).  16-byte aligned.
@@ -164,12 +166,14 @@ SLIDE_API slide_status slide_layer_step(slide_state *st, int32_t layer, const vo
  * entry (same version) else SLIDE_ERR_VERSION.
  *   forward sweep, l = 0..L-1: the BF16 copy of unit l is copied host->device
  *     into window slot l%2 (the delivery of the weights a forward would use);
- *   reverse sweep, l = L-1..0: master/m/v of l are copied host->device into
- *     its slot, fn(user, l, replicas, compute stream) produces the R gradient
- *     replicas in the slot, the fused step updates l, and master/m/v and the
- *     new BF16 copy are copied device->host; the copy of l-1 into the other
- *     slot overlaps the update of l and the write-back of l+1, handing the
- *     slot over chunk by chunk.
+ *   reverse sweep, l = L-1..0: the master of l is copied host->device into
+ *     its slot and fn(user, l, replicas, compute stream) produces the R
+ *     gradient replicas there; m and v follow chunk by chunk (chunk_bytes of
+ *     FP32 each), and the fused step updates each chunk as soon as it has
+ *     arrived; each updated chunk's master/m/v and new BF16 copy are copied
+ *     device->host right behind its update.  The copy of l-1 into the other
+ *     slot overlaps the update of l and the write-back of l+1, taking over the
+ *     slot chunk by chunk as l+1's write-back frees it.
  * Each unit is updated exactly once; every t becomes t+1.  Returns after the
  * last write-back is complete.  If fn fails or a wait times out the sweep
  * stops: units already written back carry t+1, the rest t, the state is marked
@@ -191,7 +195,8 @@ SLIDE_API slide_status slide_layer_get(slide_state *st, int32_t layer, float *ma
                              uint16_t *bf16, int64_t *step);
 
 /* Where a layer's arrays live: device pointers for the HBM residency, pinned
- * host pointers for the streamed one (owned by the state; valid until destroy). */
+ * host pointers for the streamed one (also addressable by kernels on this
+ * system's unified address space); owned by the state, valid until destroy. */
 SLIDE_API slide_status slide_layer_ptrs(slide_state *st, int32_t layer, float **master, float **m, float **v,
                               uint16_t **bf16);
 

@@ -144,14 +144,16 @@ struct GradT<uint16_t> {
     {
         return __uint_as_float((uint32_t)p[i] << 16);
     }
-    // the 8 values of vector k (16 bytes)
-    static __device__ __forceinline__ void load8(const void *base, int64_t k, float (&x)[8])
+    // the 8 values of vector k, kept raw (16 bytes) until used
+    using Raw8 = uint4;
+    static __device__ __forceinline__ Raw8 load8(const void *base, int64_t k)
     {
-        const uint4 q = __ldcs(reinterpret_cast<const uint4 *>(base) + k);
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            x[e] = (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]);
+        return __ldcs(reinterpret_cast<const uint4 *>(base) + k);
+    }
+    static __device__ __forceinline__ float at8(const Raw8 &q, int e)
+    {
+        const uint32_t word = (&q.x)[e >> 1];
+        return (e & 1) ? bf16_hi(word) : bf16_lo(word);
     }
 };
 
@@ -163,11 +165,17 @@ struct GradT<float> {
         return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
     }
     static __device__ __forceinline__ float one(const float *p, int64_t i) { return p[i]; }
-    static __device__ __forceinline__ void load8(const void *base, int64_t k, float (&x)[8])
+    struct Raw8 {
+        float4 a, b;
+    };
+    static __device__ __forceinline__ Raw8 load8(const void *base, int64_t k)
     {
-        const float4 a = __ldcs(reinterpret_cast<const float4 *>(base) + 2 * k);
-        const float4 b = __ldcs(reinterpret_cast<const float4 *>(base) + 2 * k + 1);
-        x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = b.x, x[5] = b.y, x[6] = b.z, x[7] = b.w;
+        return {__ldcs(reinterpret_cast<const float4 *>(base) + 2 * k),
+                __ldcs(reinterpret_cast<const float4 *>(base) + 2 * k + 1)};
+    }
+    static __device__ __forceinline__ float at8(const Raw8 &q, int e)
+    {
+        return e < 4 ? (&q.a.x)[e] : (&q.b.x)[e - 4];
     }
 };
 
@@ -505,14 +513,14 @@ __global__ void __launch_bounds__(kThreads) k_grad_sqnorm(SqArgs a)
     const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
     SqAcc acc;
     for (int64_t k0 = tid; k0 < nvec; k0 += stride * UNROLL) {
-        float xv[UNROLL][R][8];
+        typename GradT<G>::Raw8 raw[UNROLL][R];
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const int64_t k = k0 + (int64_t)u * stride;
             if (k < nvec) {
 #pragma unroll
                 for (int r = 0; r < R; ++r)
-                    GradT<G>::load8(a.g.p[r], k, xv[u][r]);
+                    raw[u][r] = GradT<G>::load8(a.g.p[r], k);
             }
         }
 #pragma unroll
@@ -524,7 +532,7 @@ __global__ void __launch_bounds__(kThreads) k_grad_sqnorm(SqArgs a)
                     float x[R];
 #pragma unroll
                     for (int r = 0; r < R; ++r)
-                        x[r] = xv[u][r][e];
+                        x[r] = GradT<G>::at8(raw[u][r], e);
                     acc.add(replica_mean<R>(x));
                 }
             }
@@ -660,7 +668,9 @@ cudaError_t launch_step_g(const KArgs &a, int R, bool clip, bool check, int devi
 template <typename G, int R>
 cudaError_t launch_sq_r(const SqArgs &a, int *n_partials, int device, cudaStream_t stream)
 {
-    constexpr auto kern = k_grad_sqnorm<G, R, kUnrollSq>;
+    // FP32 replicas already bring 32 bytes per replica and vector into flight
+    constexpr int kUnroll = sizeof(G) == 4 ? 1 : kUnrollSq;
+    constexpr auto kern = k_grad_sqnorm<G, R, kUnroll>;
     unsigned grid = grid_for<kern>(device, a.n, kMaxPartials);
     kern<<<grid, kThreads, 0, stream>>>(a);
     *n_partials = (int)grid;
