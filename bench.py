@@ -46,11 +46,13 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--no-variants", action="store_true",
-                    help="skip the FP32-gradient variant leg")
+                    help="skip the FP32-gradient variant, the other HBM workloads and the CPU-route legs")
     ap.add_argument("--no-streamed", action="store_true",
                     help="skip the host-streamed leg (8-layer h=8192 model, ~98 GB pinned host memory)")
     ap.add_argument("--streamed-config", type=int, default=5, choices=[4, 5])
     ap.add_argument("--streamed-steps", type=int, default=2)
+    ap.add_argument("--streamed-bf16-in-hbm", action="store_true",
+                    help="keep the BF16 copy in HBM (host holds 12 B/param); implied for config 4")
     ap.add_argument("--streamed-chunk-mib", type=int, default=64,
                     help="copy chunk of the streamed engine (the pages' 64 MiB by default)")
     ap.add_argument("--batches", type=int, default=4,
@@ -220,30 +222,32 @@ def run_reference(args):
 
 # ------------------------------------------------- FP32-gradient variant ----
 
-def run_fp32_variant(args, S, torch, synth, peak):
-    """The same workload with FP32 gradient replicas (26 + 4R bytes per
-    parameter in the fused kernel, 4R in the clip pre-pass), timed like the
-    main line: per-launch events, back to back, inputs larger than L2."""
-    from synth import workloads as W
-    w = W.config2_fp32()
+def measure_hbm_workload(args, S, torch, synth, peak, w, max_steps=500):
+    """One HBM-resident workload timed like the main line: per-launch events
+    on the launching stream, back-to-back steps over two pre-generated
+    gradient batches, inputs larger than L2."""
     n, R = w.units[0].numel, w.R
     clip = w.max_grad_norm > 0
+    gsize = 4 if w.fp32_grads else 2
     hp = S.hparams(*w.hparams_tuple())
     stream = torch.cuda.Stream()
-    st = S.slide_state_create([n], R, flags=S.SLIDE_FLAG_FP32_GRADS)
+    st = S.slide_state_create([n], R, flags=S.SLIDE_FLAG_FP32_GRADS if w.fp32_grads else 0)
     try:
         synth.dev_master(S.slide_layer_ptrs(st, 0)[0], n, w.seed, stream=stream.cuda_stream)
+        sp = synth.spec(w.seed, w.grad_kind, w.zero_prob)
+        fill = synth.dev_grad_f32 if w.fp32_grads else synth.dev_grad
         batches = []
         for b in range(2):
-            reps = [torch.empty(n + 64, dtype=torch.float32, device="cuda") for _ in range(R)]
+            reps = [torch.empty(n + 64, dtype=torch.float32 if w.fp32_grads else torch.int16, device="cuda")
+                    for _ in range(R)]
             for r, t in enumerate(reps):
-                synth.dev_grad_f32(t.data_ptr(), n, synth.spec(w.seed), 0, b + 1, r, w.grad_scale,
-                                   stream=stream.cuda_stream)
+                for (off, ln), sc in zip(w.units[0].segments(), w.tensor_scales(0)):
+                    fill(t.data_ptr() + gsize * off, ln, sp, 0, b + 1, r, sc, offset=off, stream=stream.cuda_stream)
             batches.append(reps)
         torch.cuda.synchronize()
         for i in range(max(3, args.warmup)):
             S.slide_layer_step(st, 0, batches[i % 2], hp, stream)
-        K = min(args.steps, 500)
+        K = min(args.steps, max_steps)
         ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
         for trio in ev:
             for e in trio:
@@ -262,15 +266,15 @@ def run_fp32_variant(args, S, torch, synth, peak):
         pre = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     finally:
         S.slide_state_destroy(st)
-    b_upd, b_pre = (26 + 4 * R) * n, (4 * R * n if clip else 0)
-    return {"workload": w.name, "description": w.description, "steps": K, "value": n * K / (ms * 1e-3) / 1e9,
-            "unit": UNIT, "ms_per_step": ms / K,
-            "roofline": {"bound": "hbm", "kernel": "grad_reduce_adamw_cast (FP32 replicas)",
-                         "achieved": b_upd / (upd * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
-                         "frac": b_upd / (upd * 1e-3) / 1e9 / peak, "bytes_per_param": 26 + 4 * R,
-                         "avg_launch_ms": upd},
-            "prepass": {"achieved": b_pre / (pre * 1e-3) / 1e9 if clip else None, "avg_launch_ms": pre,
-                        "bytes_per_param": 4 * R},
+    b_upd, b_pre = (26 + gsize * R) * n, (gsize * R * n if clip else 0)
+    return {"workload": w.name, "description": w.description, "params": n, "replicas": R, "steps": K,
+            "value": n * K / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms / K,
+            "hbm_gbs": (b_upd + b_pre) / (ms / K * 1e-3) / 1e9,
+            "roofline": {"bound": "hbm", "kernel": "grad_reduce_adamw_cast", "achieved": b_upd / (upd * 1e-3) / 1e9,
+                         "peak": peak, "unit": "GB/s", "frac": b_upd / (upd * 1e-3) / 1e9 / peak,
+                         "bytes_per_param": 26 + gsize * R, "avg_launch_ms": upd},
+            "prepass": ({"achieved": b_pre / (pre * 1e-3) / 1e9, "frac": b_pre / (pre * 1e-3) / 1e9 / peak,
+                         "avg_launch_ms": pre, "bytes_per_param": gsize * R} if clip else None),
             "step_roofline_frac": (b_upd + b_pre) / (ms / K * 1e-3) / 1e9 / peak}
 
 
@@ -478,7 +482,9 @@ def run_streamed(args, S, torch, synth):
     sizes = [u.numel for u in w.units]
     N = sum(sizes)
     maxn = max(sizes)
-    _, host_b = S.slide_state_bytes(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED)
+    in_hbm = args.streamed_bf16_in_hbm or args.streamed_config == 4
+    flags = S.SLIDE_FLAG_BF16_COPY_IN_HBM if in_hbm else 0
+    _, host_b = S.slide_state_bytes(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED, flags=flags)
     need = host_b + (24 << 30)
     if mem_available_bytes() < need:
         return {"workload": w.name, "skipped": f"host memory: {host_b / 1e9:.1f} GB pinned + 24 GiB headroom "
@@ -498,7 +504,7 @@ def run_streamed(args, S, torch, synth):
                           w.grad_scale)
     t0 = time.time()
     st = S.slide_state_create(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED,
-                              chunk_bytes=args.streamed_chunk_mib << 20)
+                              chunk_bytes=args.streamed_chunk_mib << 20, flags=flags)
     create_s = time.time() - t0
     try:
         for ui, u in enumerate(w.units):
@@ -519,20 +525,26 @@ def run_streamed(args, S, torch, synth):
         t0 = time.perf_counter()
         S.slide_model_step_streamed(st, fn_gen, mg, hp)
         gen_s = time.perf_counter() - t0
-        dev_b = S.slide_state_bytes(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED)[0]
+        dev_b = S.slide_state_bytes(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED, flags=flags)[0]
     finally:
         S.slide_state_destroy(st)
         del pool
     s_step = statistics.mean(times)
     G = 1e9
-    t_roof = (2 * N / (link["h2d_gbs"] * G)
-              + max(12 * N / (link["h2d_concurrent_gbs"] * G), 14 * N / (link["d2h_concurrent_gbs"] * G),
-                    26 * N / (link["bidir_gbs"] * G)))
+    if in_hbm:   # the BF16 copy's delivery and write-back stay inside HBM
+        t_roof = max(12 * N / (link["h2d_concurrent_gbs"] * G), 12 * N / (link["d2h_concurrent_gbs"] * G),
+                     24 * N / (link["bidir_gbs"] * G))
+        per_dir = 12 * N
+    else:
+        t_roof = (2 * N / (link["h2d_gbs"] * G)
+                  + max(12 * N / (link["h2d_concurrent_gbs"] * G), 14 * N / (link["d2h_concurrent_gbs"] * G),
+                        26 * N / (link["bidir_gbs"] * G)))
+        per_dir = 14 * N
     return {"workload": w.name, "description": w.description, "params": N, "replicas": w.R,
             "steps": args.streamed_steps, "s_per_step": s_step, "s_per_step_each": times,
             "gparam_s": N / s_step / 1e9, "roofline_s": t_roof, "frac": t_roof / s_step,
-            "link_bytes_per_step": {"h2d": 14 * N, "d2h": 14 * N},
-            "achieved_link_gbs_each_way": 14 * N / s_step / 1e9,
+            "link_bytes_per_step": {"h2d": per_dir, "d2h": per_dir}, "bf16_copy_in_hbm": in_hbm,
+            "achieved_link_gbs_each_way": per_dir / s_step / 1e9,
             "link": link, "host_pinned_gb": host_b / 1e9, "window_gb": dev_b / 1e9,
             "create_s": create_s, "chunk_mib": args.streamed_chunk_mib,
             "grad_callback": f"copies pre-generated replicas ({n_pool} sets, the workload's distribution) "
@@ -697,8 +709,13 @@ def run_ours(args):
 
     variant = None
     cpu_route = None
+    others = None
     if not args.no_variants and world == 1:
-        variant = run_fp32_variant(args, S, torch, synth, measured_peaks()[0])
+        from synth import workloads as W
+        peak0 = measured_peaks()[0]
+        variant = measure_hbm_workload(args, S, torch, synth, peak0, W.config2_fp32())
+        others = {W.config1().name: measure_hbm_workload(args, S, torch, synth, peak0, W.config1()),
+                  W.config3().name: measure_hbm_workload(args, S, torch, synth, peak0, W.config3(), max_steps=200)}
         cpu_route = measure_cpu_reduce_route(S, torch, synth, n, R)
     streamed = None
     if not args.no_streamed and world == 1:
@@ -763,6 +780,7 @@ def run_ours(args):
         "e2e": e2e,
         "cpu_baseline": cpu,
         "fp32_grad_variant": variant,
+        "other_hbm_workloads": others,
         "cpu_reduce_route": cpu_route,
         "streamed": streamed,
     }

@@ -94,9 +94,14 @@ enum {
                                             so the consumers' bounded wait (2 s) runs out and the step
                                             reports SLIDE_ERR_TIMEOUT through slide_layer_status; the
                                             layer's values are then undefined */
-    SLIDE_FLAG_FP32_GRADS = 4u           /* the R gradient replicas are FP32 (FP32 gradient
+    SLIDE_FLAG_FP32_GRADS = 4u,          /* the R gradient replicas are FP32 (FP32 gradient
                                             accumulation), not BF16: every replica pointer then holds
                                             n floats, and the step moves 26 + 4R bytes per parameter */
+    SLIDE_FLAG_BF16_COPY_IN_HBM = 8u     /* streamed residency: keep the BF16 compute copy in HBM
+                                            (2 B/param of device memory) instead of the pinned host
+                                            mirror; the host holds 12 B/param and the link carries
+                                            12 B/param each way per step (the delivery and the
+                                            write-back of the BF16 copy stay inside HBM) */
 };
 
 /* Adam hyper-parameters (FP32).  Valid: lr >= 0, 0 <= beta1 < 1,

@@ -36,6 +36,7 @@ SLIDE_RESIDENCY_HOST_STREAMED = 1
 SLIDE_FLAG_CHECK_FINITE = 1
 SLIDE_FLAG_TEST_PIPELINE_STALL = 2
 SLIDE_FLAG_FP32_GRADS = 4
+SLIDE_FLAG_BF16_COPY_IN_HBM = 8
 SLIDE_MAX_REPLICAS = 8
 SLIDE_DELIVER_FULL = 0
 SLIDE_DELIVER_SHARDED = 1

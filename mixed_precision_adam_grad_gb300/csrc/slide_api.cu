@@ -94,7 +94,8 @@ static slide_status check_config(const slide_config *cfg, int64_t *max_numel)
         return fail(SLIDE_ERR_INVALID_ARG, "config: window_layers must be 2 (or 0 for the default 2)");
     if (cfg->chunk_bytes < 0 || (cfg->chunk_bytes % 256) != 0)
         return fail(SLIDE_ERR_INVALID_ARG, "config: chunk_bytes must be a non-negative multiple of 256");
-    if (cfg->flags & ~(uint32_t)(SLIDE_FLAG_CHECK_FINITE | SLIDE_FLAG_TEST_PIPELINE_STALL | SLIDE_FLAG_FP32_GRADS))
+    if (cfg->flags & ~(uint32_t)(SLIDE_FLAG_CHECK_FINITE | SLIDE_FLAG_TEST_PIPELINE_STALL | SLIDE_FLAG_FP32_GRADS |
+                                 SLIDE_FLAG_BF16_COPY_IN_HBM))
         return fail(SLIDE_ERR_INVALID_ARG, "config: unknown flag bits");
     if (cfg->device < 0)
         return fail(SLIDE_ERR_INVALID_ARG, "config: device < 0");
@@ -114,6 +115,14 @@ static size_t layer_state_bytes(int64_t n)
 {
     return 3 * align_up((size_t)n * 4) + align_up((size_t)n * 2);
 }
+
+// Streamed residency with the BF16 copy in HBM: FP32 state on the host, BF16 copy on the device.
+static bool copy_in_hbm(const slide_config *cfg)
+{
+    return cfg->residency == SLIDE_RESIDENCY_HOST_STREAMED && (cfg->flags & SLIDE_FLAG_BF16_COPY_IN_HBM);
+}
+static size_t layer_fp32_bytes(int64_t n) { return 3 * align_up((size_t)n * 4); }
+static size_t layer_bf16_bytes(int64_t n) { return align_up((size_t)n * 2); }
 
 }  // namespace slide
 
@@ -137,6 +146,12 @@ slide_status slide_state_bytes(const slide_config *cfg, int64_t *device_bytes, i
     size_t dev = 0, host = 0;
     if (cfg->residency == SLIDE_RESIDENCY_HBM) {
         dev = state + (size_t)cfg->n_layers * scratch_bytes();
+    } else if (copy_in_hbm(cfg)) {
+        for (int32_t l = 0; l < cfg->n_layers; ++l) {
+            host += layer_fp32_bytes(cfg->layer_numel[l]);
+            dev += layer_bf16_bytes(cfg->layer_numel[l]);
+        }
+        dev += engine_device_bytes(*cfg, mx);
     } else {
         host = state;
         dev = engine_device_bytes(*cfg, mx);
@@ -204,6 +219,25 @@ slide_status slide_state_create(const slide_config *cfg, slide_state **out)
         }
         base = (char *)st->dev_arena;
     } else {
+        size_t mirror_bytes = 0;
+        if (copy_in_hbm(cfg)) {
+            state_bytes = 0;
+            for (int32_t l = 0; l < cfg->n_layers; ++l) {
+                state_bytes += layer_fp32_bytes(st->numel[l]);
+                mirror_bytes += layer_bf16_bytes(st->numel[l]);
+            }
+            e = cudaMalloc(&st->dev_arena, mirror_bytes > 0 ? mirror_bytes : 256);
+            if (e == cudaSuccess)
+                e = cudaMemset(st->dev_arena, 0, mirror_bytes > 0 ? mirror_bytes : 256);
+            if (e != cudaSuccess) {
+                cudaGetLastError();
+                if (st->dev_arena)
+                    cudaFree(st->dev_arena);
+                delete st;
+                return fail(SLIDE_ERR_OOM_DEVICE, "cudaMalloc of the HBM BF16 copy (" +
+                                                      std::to_string(mirror_bytes) + " bytes) failed");
+            }
+        }
         st->host_bytes = state_bytes;
         e = cudaHostAlloc(&st->host_arena, st->host_bytes > 0 ? st->host_bytes : 1, cudaHostAllocDefault);
         if (e != cudaSuccess || getenv("SLIDE_FAULT_PINNED_ALLOC")) {
@@ -212,6 +246,8 @@ slide_status slide_state_create(const slide_config *cfg, slide_state **out)
             if (e == cudaSuccess)
                 cudaFreeHost(st->host_arena);
             cudaGetLastError();
+            if (st->dev_arena)
+                cudaFree(st->dev_arena);
             delete st;
             return fail(SLIDE_ERR_OOM_HOST, std::string("cudaHostAlloc of the pinned state (") +
                                                 std::to_string(state_bytes) + " bytes) failed");
@@ -232,7 +268,7 @@ slide_status slide_state_create(const slide_config *cfg, slide_state **out)
         base = (char *)st->host_arena;
     }
 
-    size_t off = 0;
+    size_t off = 0, moff = 0;
     for (int32_t l = 0; l < cfg->n_layers; ++l) {
         LayerState &L = st->layers[l];
         const size_t n = (size_t)st->numel[l];
@@ -243,8 +279,13 @@ slide_status slide_state_create(const slide_config *cfg, slide_state **out)
         off += align_up(n * 4);
         L.v = (float *)(base + off);
         off += align_up(n * 4);
-        L.w = (uint16_t *)(base + off);
-        off += align_up(n * 2);
+        if (copy_in_hbm(cfg)) {
+            L.w = (uint16_t *)((char *)st->dev_arena + moff);
+            moff += layer_bf16_bytes((int64_t)n);
+        } else {
+            L.w = (uint16_t *)(base + off);
+            off += align_up(n * 2);
+        }
     }
     if (cfg->residency == SLIDE_RESIDENCY_HBM) {
         for (int32_t l = 0; l < cfg->n_layers; ++l) {
@@ -258,6 +299,8 @@ slide_status slide_state_create(const slide_config *cfg, slide_state **out)
         rc = engine_create(st);
         if (rc != SLIDE_OK) {
             cudaFreeHost(st->host_arena);
+            if (st->dev_arena)
+                cudaFree(st->dev_arena);
             delete st;
             return rc;
         }
@@ -392,7 +435,7 @@ slide_status slide_layer_set(slide_state *st, int32_t layer, const float *master
         uint16_t *w_d = L.w;
         if (st->cfg.residency == SLIDE_RESIDENCY_HOST_STREAMED) {
             e = cudaHostGetDevicePointer((void **)&th_d, L.theta, 0);
-            if (e == cudaSuccess)
+            if (e == cudaSuccess && !copy_in_hbm(&st->cfg))
                 e = cudaHostGetDevicePointer((void **)&w_d, L.w, 0);
             if (e != cudaSuccess)
                 return fail_cuda(e, "cudaHostGetDevicePointer in slide_layer_set");

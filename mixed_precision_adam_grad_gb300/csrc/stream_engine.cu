@@ -26,7 +26,9 @@
 // (grad_reduce_adamw_cast), so per parameter and step the link moves
 //   host -> device: 2 B (BF16 delivery, forward sweep) + 12 B (master, m, v)
 //   device -> host: 12 B (master, m, v) + 2 B (new BF16 copy)
-// and the R gradient replicas never leave HBM.
+// and the R gradient replicas never leave HBM.  With the BF16 copy kept in
+// HBM (SLIDE_FLAG_BF16_COPY_IN_HBM) its delivery and write-back are device-to-
+// device copies and the link carries 12 B each way.
 //
 // A unit's arrays are split into chunks of chunk_bytes of FP32 (the BF16
 // copy and the replicas use the same element ranges).  Schedule of one step,
@@ -285,7 +287,7 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
             const Chunk c = E->chunk(U.n, k);
             e = cudaStreamWaitEvent(E->s_h2d, s.freed[kW][k], 0);
             if (e == cudaSuccess)
-                e = cudaMemcpyAsync(s.w + c.off, U.w + c.off, (size_t)c.len * 2, cudaMemcpyHostToDevice, E->s_h2d);
+                e = cudaMemcpyAsync(s.w + c.off, U.w + c.off, (size_t)c.len * 2, cudaMemcpyDefault, E->s_h2d);
         }
     }
     if (e == cudaSuccess)
@@ -393,7 +395,7 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
             if (e == cudaSuccess && k == 0)
                 e = cudaEventRecord(E->d2h_begin[l], E->s_d2h);
             if (e == cudaSuccess)
-                e = cudaMemcpyAsync(U.w + c.off, s.w + c.off, (size_t)c.len * 2, cudaMemcpyDeviceToHost, E->s_d2h);
+                e = cudaMemcpyAsync(U.w + c.off, s.w + c.off, (size_t)c.len * 2, cudaMemcpyDefault, E->s_d2h);
             if (e == cudaSuccess)
                 e = cudaEventRecord(s.freed[kW][k], E->s_d2h);
             for (int r = 0; r < 3 && e == cudaSuccess; ++r) {

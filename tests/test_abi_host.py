@@ -90,6 +90,19 @@ def test_accounting_streamed_window_independent_of_N(S):
     assert d2 == 2 * slot
 
 
+def test_accounting_streamed_bf16_copy_in_hbm(S):
+    """With the BF16 copy in HBM the host holds 12 B/param (FP32 master and
+    two moments) and the device adds 2 B/param to the window."""
+    many = [778_567_680] + [330_311_680] * 40 + [778_567_680]
+    N = sum(many)
+    d0, h0 = S.slide_state_bytes(many, 4, residency=S.SLIDE_RESIDENCY_HOST_STREAMED)
+    d1, h1 = S.slide_state_bytes(many, 4, residency=S.SLIDE_RESIDENCY_HOST_STREAMED,
+                                 flags=S.SLIDE_FLAG_BF16_COPY_IN_HBM)
+    assert 12 * N <= h1 <= 12 * N + 3 * A * len(many)
+    assert d1 == d0 + sum(al(2 * n) for n in many)
+    assert h0 - h1 == sum(al(2 * n) for n in many)
+
+
 @pytest.mark.parametrize("kw,msg", [
     (dict(layer_numel=[10], n_replicas=0), "n_replicas"),
     (dict(layer_numel=[10], n_replicas=9), "n_replicas"),
@@ -97,7 +110,7 @@ def test_accounting_streamed_window_independent_of_N(S):
     (dict(layer_numel=[10], n_replicas=1, residency=7), "residency"),
     (dict(layer_numel=[10], n_replicas=1, chunk_bytes=100), "chunk_bytes"),
     (dict(layer_numel=[10], n_replicas=1, window_layers=3), "window_layers"),
-    (dict(layer_numel=[10], n_replicas=1, flags=8), "flag"),
+    (dict(layer_numel=[10], n_replicas=1, flags=16), "flag"),
     (dict(layer_numel=[], n_replicas=1), "n_layers"),
 ])
 def test_config_validation_without_gpu(S, kw, msg):

@@ -32,27 +32,19 @@ def test_normals_are_standard_normal():
 
 def test_own_log_and_sincos_close_to_libm():
     """Box-Muller's log and sin/cos are this generator's own (bit-identical on
-    host and GPU); they must still be close to the true functions."""
-    u = synth.normals(1, 1, 0)  # build/load
-    del u
-    lib = synth.host()
-    # a normal's magnitude depends on log(u1) and cos(2 pi u2): compare the
-    # generator's normals with the same pair computed by numpy in double
-    import ctypes as C
+    host and GPU); the normals they give must still be close to the ones the
+    true functions give for the same Philox words (computed here in double)."""
     n = 4096
-    ctr0 = 0
     zs = synth.normals(4 * n, seed=11, tag=7, a=1, b=2, c=3).astype(np.float64)
     ref = []
     for j in range(n):
-        w = synth.philox([(ctr0 + j) & 0xFFFFFFFF, 1, 2, 3], [11, 7])
+        w = synth.philox([j, 1, 2, 3], [11, 7])
         for a, b in ((w[0], w[1]), (w[2], w[3])):
             u1 = ((a >> 8) + 1) * 2.0 ** -24
             u2 = ((b >> 8) + 1) * 2.0 ** -24
             r = np.sqrt(-2 * np.log(u1))
             ref += [r * np.cos(2 * np.pi * u2), r * np.sin(2 * np.pi * u2)]
-    ref = np.array(ref)
-    assert np.max(np.abs(zs - ref)) < 2e-6 * 6
-    del lib, C
+    assert np.max(np.abs(zs - np.array(ref))) < 1.2e-5
 
 
 def test_fill_and_gather_agree_with_offsets():
