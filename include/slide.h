@@ -199,9 +199,10 @@ SLIDE_API slide_status slide_layer_set(slide_state *st, int32_t layer, const flo
 SLIDE_API slide_status slide_layer_get(slide_state *st, int32_t layer, float *master, float *m, float *v,
                              uint16_t *bf16, int64_t *step);
 
-/* Where a layer's arrays live: device pointers for the HBM residency, pinned
- * host pointers for the streamed one (also addressable by kernels on this
- * system's unified address space); owned by the state, valid until destroy. */
+/* Where a layer's arrays live: device pointers for the HBM residency; for the
+ * streamed one pinned host pointers (also addressable by kernels through the
+ * unified address space), except the BF16 copy, which is a device pointer
+ * with SLIDE_FLAG_BF16_COPY_IN_HBM.  Owned by the state, valid until destroy. */
 SLIDE_API slide_status slide_layer_ptrs(slide_state *st, int32_t layer, float **master, float **m, float **v,
                               uint16_t **bf16);
 

@@ -668,9 +668,7 @@ cudaError_t launch_step_g(const KArgs &a, int R, bool clip, bool check, int devi
 template <typename G, int R>
 cudaError_t launch_sq_r(const SqArgs &a, int *n_partials, int device, cudaStream_t stream)
 {
-    // FP32 replicas already bring 32 bytes per replica and vector into flight
-    constexpr int kUnroll = sizeof(G) == 4 ? 1 : kUnrollSq;
-    constexpr auto kern = k_grad_sqnorm<G, R, kUnroll>;
+    constexpr auto kern = k_grad_sqnorm<G, R, kUnrollSq>;
     unsigned grid = grid_for<kern>(device, a.n, kMaxPartials);
     kern<<<grid, kThreads, 0, stream>>>(a);
     *n_partials = (int)grid;
