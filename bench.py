@@ -40,8 +40,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3],
-                    help="HBM-resident workload (1: h2560 R1, 2: h2560 R4 clip, 3: h5120 R8)")
+    ap.add_argument("--workload", default="h2560_R4_clip", choices=["h2560_R1", "h2560_R4_clip", "h5120_R8_logscale"],
+                    help="HBM-resident workload of the main line")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=100)
@@ -49,10 +49,11 @@ def parse_args():
                     help="skip the FP32-gradient variant, the other HBM workloads and the CPU-route legs")
     ap.add_argument("--no-streamed", action="store_true",
                     help="skip the host-streamed leg (8-layer h=8192 model, ~98 GB pinned host memory)")
-    ap.add_argument("--streamed-config", type=int, default=5, choices=[4, 5])
+    ap.add_argument("--streamed-workload", default="h8192x8_streamed",
+                    choices=["h8192x8_streamed", "h5120x40_streamed"])
     ap.add_argument("--streamed-steps", type=int, default=2)
     ap.add_argument("--streamed-bf16-in-hbm", action="store_true",
-                    help="keep the BF16 copy in HBM (host holds 12 B/param); implied for config 4")
+                    help="keep the BF16 copy in HBM (host holds 12 B/param); implied for h5120x40_streamed")
     ap.add_argument("--streamed-chunk-mib", type=int, default=64,
                     help="copy chunk of the streamed engine (the pages' 64 MiB by default)")
     ap.add_argument("--batches", type=int, default=4,
@@ -154,13 +155,9 @@ def max_over_ranks(x: float, dist=None) -> float:
     return float(t.item())
 
 
-def workload(cfg):
+def workload(name):
     from synth import workloads as W
-    return W.ALL[cfg]()
-
-
-def workload_any(cfg):
-    return workload(cfg)
+    return W.ALL[name]()
 
 
 # ------------------------------------------------------------ oracle ----
@@ -196,7 +193,7 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
-    w = workload(args.config)
+    w = workload(args.workload)
     # calibrate, then size each step's sample so the whole run takes ~2 minutes
     rate, _, _ = oracle_sample_rate(w, 1 << 20, 0.5, 3, seed_offset=1000)
     per_step_s = 120.0 / (args.steps + args.warmup)
@@ -478,11 +475,11 @@ def run_streamed(args, S, torch, synth):
     so the time is the engine's copies and update; one more step with the
     on-the-fly generator as the callback is reported beside it."""
     import ctypes as C
-    w = workload_any(args.streamed_config)
+    w = workload(args.streamed_workload)
     sizes = [u.numel for u in w.units]
     N = sum(sizes)
     maxn = max(sizes)
-    in_hbm = args.streamed_bf16_in_hbm or args.streamed_config == 4
+    in_hbm = args.streamed_bf16_in_hbm or args.streamed_workload == "h5120x40_streamed"
     flags = S.SLIDE_FLAG_BF16_COPY_IN_HBM if in_hbm else 0
     _, host_b = S.slide_state_bytes(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED, flags=flags)
     need = host_b + (24 << 30)
@@ -570,7 +567,7 @@ def run_ours(args):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
-    w = workload(args.config)
+    w = workload(args.workload)
     n = w.units[0].numel
     R = w.R
     clip = w.max_grad_norm > 0
@@ -713,9 +710,10 @@ def run_ours(args):
     if not args.no_variants and world == 1:
         from synth import workloads as W
         peak0 = measured_peaks()[0]
-        variant = measure_hbm_workload(args, S, torch, synth, peak0, W.config2_fp32())
-        others = {W.config1().name: measure_hbm_workload(args, S, torch, synth, peak0, W.config1()),
-                  W.config3().name: measure_hbm_workload(args, S, torch, synth, peak0, W.config3(), max_steps=200)}
+        variant = measure_hbm_workload(args, S, torch, synth, peak0, W.h2560_r4_clip_fp32grads())
+        others = {name: measure_hbm_workload(args, S, torch, synth, peak0, W.ALL[name](),
+                                             max_steps=200 if name == "h5120_R8_logscale" else 500)
+                  for name in W.HBM_RESIDENT if name != args.workload}
         cpu_route = measure_cpu_reduce_route(S, torch, synth, n, R)
     streamed = None
     if not args.no_streamed and world == 1:

@@ -99,12 +99,12 @@ class Workload:
         return (self.lr, self.beta1, self.beta2, self.eps, self.weight_decay, self.max_grad_norm)
 
 
-def config1() -> Workload:
+def h2560_r1() -> Workload:
     return Workload("h2560_R1", [Unit("layer", h2560_layer())], R=1, steps=3, seed=0,
                     description="one h=2560 decoder layer (100,930,560 params), R=1, 3 AdamW steps")
 
 
-def config2() -> Workload:
+def h2560_r4_clip() -> Workload:
     return Workload("h2560_R4_clip", [Unit("layer", h2560_layer())], R=4, steps=10, seed=1,
                     max_grad_norm=1.0, prewarm_steps=5,
                     description="one h=2560 decoder layer, R=4 replicas averaged in-kernel, "
@@ -112,14 +112,14 @@ def config2() -> Workload:
                                 "then 10 steps")
 
 
-def config3() -> Workload:
+def h5120_r8_logscale() -> Workload:
     return Workload("h5120_R8_logscale", [Unit("layer", h5120_layer())], R=8, steps=20, seed=2,
                     per_tensor_scale=True,
                     description="one h=5120 decoder layer (330,311,680 params), R=8, per-tensor "
                                 "gradient scale log-uniform in [1e-5, 1e-2], 20 steps")
 
 
-def config4() -> Workload:
+def h5120x40_streamed() -> Workload:
     units = ([Unit("embed", [("embed", 152064 * 5120)])]
              + [Unit(f"layer{i}", h5120_layer()) for i in range(40)]
              + [Unit("head", [("head", 152064 * 5120)])])
@@ -128,7 +128,7 @@ def config4() -> Workload:
                                 "(14,769,602,560 params), host-resident, 2-unit HBM window, R=4")
 
 
-def config5() -> Workload:
+def h8192x8_streamed() -> Workload:
     units = [Unit(f"layer{i}", h8192_layer()) for i in range(8)]
     return Workload("h8192x8_streamed", units, R=8, steps=2, seed=4, streamed=True,
                     grad_kind=GRAD_STUDENT3, zero_prob=0.001,
@@ -137,13 +137,16 @@ def config5() -> Workload:
                                 "0.1% exact zeros")
 
 
-def config2_fp32() -> Workload:
-    w = config2()
+def h2560_r4_clip_fp32grads() -> Workload:
+    w = h2560_r4_clip()
     w.name = "h2560_R4_clip_fp32grads"
     w.fp32_grads = True
-    w.description = ("config 2 with FP32 gradient replicas (FP32 gradient accumulation): "
+    w.description = ("the h=2560 R=4 clipped layer with FP32 gradient replicas (FP32 gradient accumulation): "
                      "26 + 4R bytes per parameter")
     return w
 
 
-ALL = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
+ALL = {f().name: f for f in (h2560_r1, h2560_r4_clip, h5120_r8_logscale, h5120x40_streamed, h8192x8_streamed,
+                             h2560_r4_clip_fp32grads)}
+HBM_RESIDENT = ("h2560_R1", "h2560_R4_clip", "h5120_R8_logscale")
+STREAMED = ("h8192x8_streamed", "h5120x40_streamed")

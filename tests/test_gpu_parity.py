@@ -346,8 +346,8 @@ def run_full_size(S, w, n_samples=200_000):
         S.slide_state_destroy(st)
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3, "2-fp32"])
-def test_full_size_workload_sampled(S, cfg):
-    w = W.config2_fp32() if cfg == "2-fp32" else W.ALL[cfg]()
+@pytest.mark.parametrize("name", ["h2560_R1", "h2560_R4_clip", "h5120_R8_logscale", "h2560_R4_clip_fp32grads"])
+def test_full_size_workload_sampled(S, name):
+    w = W.ALL[name]()
     rep = run_full_size(S, w)
     print(rep)

@@ -74,9 +74,9 @@ def test_student_t3_with_exact_zeros():
 
 
 def test_workload_sizes():
-    assert W.config1().numel == 100_930_560
-    assert W.config3().numel == 330_311_680
-    assert W.config4().numel == 14_769_602_560
-    assert W.config5().numel == 7_021_395_968
-    s = W.config3().tensor_scales(0)
+    assert W.h2560_r1().numel == 100_930_560
+    assert W.h5120_r8_logscale().numel == 330_311_680
+    assert W.h5120x40_streamed().numel == 14_769_602_560
+    assert W.h8192x8_streamed().numel == 7_021_395_968
+    s = W.h5120_r8_logscale().tensor_scales(0)
     assert len(s) == 9 and all(1e-5 <= x <= 1e-2 for x in s) and len(set(s)) == 9
