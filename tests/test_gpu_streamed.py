@@ -242,17 +242,17 @@ def _host_view(ptr, n, ctype, dtype):
     return np.ctypeslib.as_array((ctype * n).from_address(ptr)).view(dtype)
 
 
-@pytest.mark.parametrize("cfg", [5, 4])
-def test_streamed_full_size_sampled(S, cfg):
+@pytest.mark.parametrize("name", ["h8192x8_streamed", "h5120x40_streamed"])
+def test_streamed_full_size_sampled(S, name):
     """The full host-streamed workloads, sampled: every checked unit's sampled
     elements against the oracle after each step; the BF16 copy equals bf16 of
     the master; t advanced once per step.  The 40-layer h5120 model (14.8 B
     parameters) keeps its BF16 copy in HBM so that its 12 B/param of FP32
     state fits the host; the sampled elements are read through views of the
     pinned state, without copying it."""
-    w = W.ALL[cfg]()
+    w = W.ALL[name]()
     sizes = [u.numel for u in w.units]
-    flags = S.SLIDE_FLAG_BF16_COPY_IN_HBM if cfg == 4 else 0
+    flags = S.SLIDE_FLAG_BF16_COPY_IN_HBM if name == "h5120x40_streamed" else 0
     _, host_b = S.slide_state_bytes(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED, flags=flags)
     if _mem_available() < host_b + (24 << 30):
         pytest.skip(f"host memory: needs {host_b / 2**30:.0f} GiB pinned + 24 GiB headroom, "
