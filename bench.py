@@ -51,7 +51,7 @@ def parse_args():
                     help="skip the host-streamed leg (8-layer h=8192 model, ~98 GB pinned host memory)")
     ap.add_argument("--streamed-workload", default="h8192x8_streamed",
                     choices=["h8192x8_streamed", "h5120x40_streamed"])
-    ap.add_argument("--streamed-steps", type=int, default=2)
+    ap.add_argument("--streamed-steps", type=int, default=5)
     ap.add_argument("--streamed-bf16-in-hbm", action="store_true",
                     help="keep the BF16 copy in HBM (host holds 12 B/param); implied for h5120x40_streamed")
     ap.add_argument("--streamed-chunk-mib", type=int, default=64,
@@ -415,6 +415,67 @@ def link_probe(torch, nbytes=1 << 30, reps=20):
     return out
 
 
+def link_monitor(torch, seconds=2.0, chunk=64 << 20, slots=8):
+    """Both directions of the host link kept busy for `seconds` with
+    back-to-back pinned <-> device copies of `chunk` bytes, every copy timed
+    by its own pair of events.  The per-copy rates over time show whether the
+    link held its rate for the whole window: on a host shared with other
+    work it can drop for stretches of a few hundred ms, which a median-based
+    probe hides.  Rates in GB/s; a copy is "slow" below 0.8 x the median."""
+    h_src = torch.empty(slots, chunk, dtype=torch.uint8, pin_memory=True)
+    h_dst = torch.empty(slots, chunk, dtype=torch.uint8, pin_memory=True)
+    d_dst = torch.empty(slots, chunk, dtype=torch.uint8, device="cuda")
+    d_src = torch.empty(slots, chunk, dtype=torch.uint8, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    n = max(8, int(seconds * 175e9 / chunk))
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(n + 1)] for _ in range(2)]
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    start.record(s1)
+    s2.wait_event(start)
+    ev[0][0].record(s1)
+    ev[1][0].record(s2)
+    for i in range(n):
+        j = i % slots
+        with torch.cuda.stream(s1):
+            d_dst[j].copy_(h_src[j], non_blocking=True)
+            ev[0][i + 1].record(s1)
+        with torch.cuda.stream(s2):
+            h_dst[j].copy_(d_src[j], non_blocking=True)
+            ev[1][i + 1].record(s2)
+    torch.cuda.synchronize()
+    out = {"seconds": seconds, "copy_mib": chunk >> 20}
+    for d, name in ((0, "h2d"), (1, "d2h")):
+        ms = [ev[d][i].elapsed_time(ev[d][i + 1]) for i in range(n)]
+        gbs = [chunk / (t * 1e-3) / 1e9 for t in ms]
+        med = statistics.median(gbs)
+        srt = sorted(gbs)
+        slow_ms = sum(t for t, g in zip(ms, gbs) if g < 0.8 * med)
+        longest = run = 0.0
+        for t, g in zip(ms, gbs):
+            run = run + t if g < 0.8 * med else 0.0
+            longest = max(longest, run)
+        out[name] = {"median_gbs": med, "p5_gbs": srt[len(srt) // 20], "min_gbs": srt[0],
+                     "slow_ms": slow_ms, "longest_slow_stretch_ms": longest, "window_ms": sum(ms)}
+    del h_src, h_dst, d_dst, d_src
+    return out
+
+
+def unit_spread(units):
+    """Longest unit copy-in of a streamed step against the median unit (the
+    first and last units of the sweep excluded: they have no neighbour on one
+    side): a ratio near 1 means every unit met the same link rate."""
+    import math
+    inner = [(i, u["h2d_end"] - u["h2d_begin"]) for i, u in enumerate(units[1:-1], 1)
+             if not math.isnan(u["h2d_begin"])]
+    if not inner:
+        return {"unit_max_over_median": None, "slowest_unit": None}
+    med = statistics.median(t for _, t in inner)
+    i, t = max(inner, key=lambda x: x[1])
+    return {"unit_max_over_median": t / med if med > 0 else None, "slowest_unit": i,
+            "median_unit_copy_in_ms": med}
+
+
 def _union(intervals):
     out = []
     for a, b in sorted(intervals):
@@ -487,6 +548,7 @@ def run_streamed(args, S, torch, synth):
         return {"workload": w.name, "skipped": f"host memory: {host_b / 1e9:.1f} GB pinned + 24 GiB headroom "
                                                 f"needed, {mem_available_bytes() / 1e9:.1f} GB available"}
     link = link_probe(torch)
+    monitor_before = link_monitor(torch)
     n_pool = 2
     sp = synth.spec(w.seed, w.grad_kind, w.zero_prob)
     pool = [torch.empty(maxn + 64, dtype=torch.int16, device="cuda") for _ in range(n_pool * w.R)]
@@ -510,14 +572,19 @@ def run_streamed(args, S, torch, synth):
         hp = S.hparams(*w.hparams_tuple())
         fn_pool, fn_gen = synth.pool_grad_fn_address(), synth.grad_fn_address()
         S.slide_model_step_streamed(st, fn_pool, pg, hp)          # warm-up step
-        times = []
+        times, per_step, tls = [], [], []
         for k in range(args.streamed_steps):
             pg.step = 1 + k
             t0 = time.perf_counter()
             S.slide_model_step_streamed(st, fn_pool, pg, hp)      # returns after the last write-back
             times.append(time.perf_counter() - t0)
-        units_tl, fwd_end = S.slide_streamed_timeline(st)
-        overlap = timeline_overlap(units_tl, fwd_end)
+            units_tl, fwd_end = S.slide_streamed_timeline(st)
+            tls.append((units_tl, fwd_end))
+            per_step.append(dict(s=times[-1], **unit_spread(units_tl)))
+        monitor_after = link_monitor(torch)
+        fastest, slowest = times.index(min(times)), times.index(max(times))
+        overlap_fast = timeline_overlap(*tls[fastest])
+        overlap_slow = timeline_overlap(*tls[slowest])
         delivery = measure_delivery(S, torch, st, 0, sizes[0], w.R)
         t0 = time.perf_counter()
         S.slide_model_step_streamed(st, fn_gen, mg, hp)
@@ -526,7 +593,7 @@ def run_streamed(args, S, torch, synth):
     finally:
         S.slide_state_destroy(st)
         del pool
-    s_step = statistics.mean(times)
+    s_step = statistics.median(times)
     G = 1e9
     if in_hbm:   # the BF16 copy's delivery and write-back stay inside HBM
         t_roof = max(12 * N / (link["h2d_concurrent_gbs"] * G), 12 * N / (link["d2h_concurrent_gbs"] * G),
@@ -539,17 +606,20 @@ def run_streamed(args, S, torch, synth):
         per_dir = 14 * N
     return {"workload": w.name, "description": w.description, "params": N, "replicas": w.R,
             "steps": args.streamed_steps, "s_per_step": s_step, "s_per_step_each": times,
+            "s_per_step_min": min(times), "s_per_step_mean": statistics.mean(times),
             "gparam_s": N / s_step / 1e9, "roofline_s": t_roof, "frac": t_roof / s_step,
+            "frac_fastest_step": t_roof / min(times), "per_step": per_step,
             "link_bytes_per_step": {"h2d": per_dir, "d2h": per_dir}, "bf16_copy_in_hbm": in_hbm,
             "achieved_link_gbs_each_way": per_dir / s_step / 1e9,
-            "link": link, "host_pinned_gb": host_b / 1e9, "window_gb": dev_b / 1e9,
+            "link": link, "link_monitor_before": monitor_before, "link_monitor_after": monitor_after,
+            "host_pinned_gb": host_b / 1e9, "window_gb": dev_b / 1e9,
             "create_s": create_s, "chunk_mib": args.streamed_chunk_mib,
             "grad_callback": f"copies pre-generated replicas ({n_pool} sets, the workload's distribution) "
                              "from HBM into the window",
             "s_per_step_with_generator_callback": gen_s,
-            "timeline_last_step": overlap,
+            "timeline_fastest_step": overlap_fast, "timeline_slowest_step": overlap_slow,
             "bf16_delivery": delivery,
-            "timing": "host wall clock around each synchronous model step"}
+            "timing": "host wall clock around each synchronous model step; s_per_step is the median"}
 
 
 # --------------------------------------------------------------- ours ----

@@ -27,13 +27,15 @@
 //   host -> device: 2 B (BF16 delivery, forward sweep) + 12 B (master, m, v)
 //   device -> host: 12 B (master, m, v) + 2 B (new BF16 copy)
 // and the R gradient replicas never leave HBM.  With the BF16 copy kept in
-// HBM (SLIDE_FLAG_BF16_COPY_IN_HBM) its delivery and write-back are device-to-
-// device copies and the link carries 12 B each way.
+// HBM (SLIDE_FLAG_BF16_COPY_IN_HBM) the window has no BF16 slot: the update
+// writes the unit's resident copy in place, there is nothing to deliver or
+// write back, and the link carries 12 B each way.
 //
 // A unit's arrays are split into chunks of chunk_bytes of FP32 (the BF16
 // copy and the replicas use the same element ranges).  Schedule of one step,
 // all enqueued up front, then one bounded host wait per stream:
-//  forward sweep (H2D stream): the BF16 copy of unit l -> slot l%2, in order;
+//  forward sweep (H2D stream): the BF16 copy of unit l -> slot l%2, in order
+//                  (skipped when the copy is kept in HBM);
 //  reverse sweep, l = L-1 .. 0, slot s = l%2:
 //    H2D stream:     the master of l, then its m and v chunk by chunk; every
 //                    chunk first waits for the write-back of the same bytes by
@@ -79,9 +81,12 @@ struct Slot {
 
 size_t grad_bytes(const slide_config &cfg) { return (cfg.flags & SLIDE_FLAG_FP32_GRADS) ? 4 : 2; }
 
-size_t slot_bytes(int64_t maxn, int R, size_t gsize)
+// The window holds the BF16 copy only when the copy lives in host memory.
+bool bf16_slot(const slide_config &cfg) { return (cfg.flags & SLIDE_FLAG_BF16_COPY_IN_HBM) == 0; }
+
+size_t slot_bytes(int64_t maxn, int R, size_t gsize, bool w_slot)
 {
-    return 3 * align_up((size_t)maxn * 4) + align_up((size_t)maxn * 2) +
+    return 3 * align_up((size_t)maxn * 4) + (w_slot ? align_up((size_t)maxn * 2) : 0) +
            align_up((size_t)maxn * gsize) * (size_t)R + scratch_bytes();
 }
 
@@ -117,7 +122,7 @@ struct StreamEngine {
 
 size_t engine_device_bytes(const slide_config &cfg, int64_t max_numel)
 {
-    return kSlots * slot_bytes(max_numel, cfg.n_replicas, grad_bytes(cfg));
+    return kSlots * slot_bytes(max_numel, cfg.n_replicas, grad_bytes(cfg), bf16_slot(cfg));
 }
 
 static void destroy_engine_objects(StreamEngine *E)
@@ -175,8 +180,10 @@ slide_status engine_create(slide_state *st)
             s.arr[r] = (float *)p;
             p += align_up((size_t)maxn * 4);
         }
-        s.w = (uint16_t *)p;
-        p += align_up((size_t)maxn * 2);
+        if (bf16_slot(st->cfg)) {
+            s.w = (uint16_t *)p;
+            p += align_up((size_t)maxn * 2);
+        }
         for (int r = 0; r < R; ++r) {
             s.g[r] = p;
             p += align_up((size_t)maxn * E->gsize);
@@ -271,6 +278,7 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
     const bool check = (st->cfg.flags & SLIDE_FLAG_CHECK_FINITE) != 0;
     const bool stall = (st->cfg.flags & SLIDE_FLAG_TEST_PIPELINE_STALL) != 0;
     const bool f32g = (st->cfg.flags & SLIDE_FLAG_FP32_GRADS) != 0;
+    const bool w_slot = bf16_slot(st->cfg);  // false: the BF16 copy is updated in place in HBM
     cudaError_t e = cudaSuccess;
     slide_status rc = SLIDE_OK;
     int done_units = 0;  // units whose update and write-back were enqueued (from L-1 down)
@@ -279,15 +287,17 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
         E->recorded[l] = 0;
     e = cudaEventRecord(E->step_start, E->s_h2d);
 
-    // forward sweep: deliver the BF16 copy of every unit, in order
-    for (int l = 0; l < L && e == cudaSuccess; ++l) {
+    // forward sweep: deliver the BF16 copy of every unit, in order (a copy
+    // kept in HBM is already where the forward pass reads it)
+    for (int l = 0; l < L && w_slot && e == cudaSuccess; ++l) {
         Slot &s = E->slots[l % kSlots];
         const LayerState &U = st->layers[l];
         for (int k = 0; k < E->n_chunks(U.n) && e == cudaSuccess; ++k) {
             const Chunk c = E->chunk(U.n, k);
             e = cudaStreamWaitEvent(E->s_h2d, s.freed[kW][k], 0);
             if (e == cudaSuccess)
-                e = cudaMemcpyAsync(s.w + c.off, U.w + c.off, (size_t)c.len * 2, cudaMemcpyDefault, E->s_h2d);
+                e = cudaMemcpyAsync(s.w + c.off, U.w + c.off, (size_t)c.len * 2, cudaMemcpyHostToDevice,
+                                    E->s_h2d);
         }
     }
     if (e == cudaSuccess)
@@ -369,7 +379,7 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
         for (int k = 0; k < K && e == cudaSuccess; ++k) {
             const Chunk c = E->chunk(U.n, k);
             e = cudaStreamWaitEvent(E->s_comp, s.mv_landed[k], 0);
-            if (e == cudaSuccess)
+            if (e == cudaSuccess && w_slot)
                 e = cudaStreamWaitEvent(E->s_comp, s.freed[kW][k], 0);
             if (e != cudaSuccess)
                 break;
@@ -377,7 +387,7 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
             for (int r = 0; r < R; ++r)
                 gk.p[r] = (const char *)s.g[r] + (size_t)c.off * E->gsize;
             e = launch_grad_reduce_adamw_cast(gk, R, c.len, s.arr[0] + c.off, s.arr[1] + c.off, s.arr[2] + c.off,
-                                              s.w + c.off, sc, &s.scratch, n_partials,
+                                              (w_slot ? s.w : U.w) + c.off, sc, &s.scratch, n_partials,
                                               clip ? hp.max_grad_norm : 0.0f, check, st->device, E->s_comp, stall,
                                               f32g);
             if (e == cudaSuccess)
@@ -394,10 +404,11 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
             e = cudaStreamWaitEvent(E->s_d2h, s.upd_done[k], 0);
             if (e == cudaSuccess && k == 0)
                 e = cudaEventRecord(E->d2h_begin[l], E->s_d2h);
-            if (e == cudaSuccess)
-                e = cudaMemcpyAsync(U.w + c.off, s.w + c.off, (size_t)c.len * 2, cudaMemcpyDefault, E->s_d2h);
-            if (e == cudaSuccess)
-                e = cudaEventRecord(s.freed[kW][k], E->s_d2h);
+            if (e == cudaSuccess && w_slot) {
+                e = cudaMemcpyAsync(U.w + c.off, s.w + c.off, (size_t)c.len * 2, cudaMemcpyDeviceToHost, E->s_d2h);
+                if (e == cudaSuccess)
+                    e = cudaEventRecord(s.freed[kW][k], E->s_d2h);
+            }
             for (int r = 0; r < 3 && e == cudaSuccess; ++r) {
                 e = cudaMemcpyAsync(dst[r] + c.off, s.arr[r] + c.off, (size_t)c.len * 4, cudaMemcpyDeviceToHost,
                                     E->s_d2h);

@@ -92,14 +92,15 @@ def test_accounting_streamed_window_independent_of_N(S):
 
 def test_accounting_streamed_bf16_copy_in_hbm(S):
     """With the BF16 copy in HBM the host holds 12 B/param (FP32 master and
-    two moments) and the device adds 2 B/param to the window."""
+    two moments); the device holds 2 B/param of BF16 copy and the window
+    drops its two BF16 slots (the update writes the resident copy in place)."""
     many = [778_567_680] + [330_311_680] * 40 + [778_567_680]
     N = sum(many)
     d0, h0 = S.slide_state_bytes(many, 4, residency=S.SLIDE_RESIDENCY_HOST_STREAMED)
     d1, h1 = S.slide_state_bytes(many, 4, residency=S.SLIDE_RESIDENCY_HOST_STREAMED,
                                  flags=S.SLIDE_FLAG_BF16_COPY_IN_HBM)
     assert 12 * N <= h1 <= 12 * N + 3 * A * len(many)
-    assert d1 == d0 + sum(al(2 * n) for n in many)
+    assert d1 == d0 + sum(al(2 * n) for n in many) - 2 * al(2 * max(many))
     assert h0 - h1 == sum(al(2 * n) for n in many)
 
 

@@ -62,3 +62,24 @@ def test_warmup_minimum():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--warmup", "2"],
                        capture_output=True, text=True, timeout=120)
     assert r.returncode != 0
+
+
+def test_unit_spread_and_overlap():
+    """Per-step spread of the unit copy-in times and the busy/overlap summary
+    of a streamed timeline, on a hand-made timeline with one slow unit."""
+    nan = float("nan")
+    units = []
+    t = 10.0
+    for i, dur in enumerate([30.0, 20.0, 20.0, 60.0, 20.0, 25.0]):
+        units.append({"h2d_begin": t, "master_landed": t + 5, "h2d_end": t + dur, "update_end": t + dur,
+                      "d2h_begin": t + 6, "d2h_end": t + dur + 4})
+        t += dur
+    sp = bench.unit_spread(units)
+    assert sp["slowest_unit"] == 3
+    assert sp["median_unit_copy_in_ms"] == 20.0
+    assert sp["unit_max_over_median"] == 3.0
+    assert bench.unit_spread(units[:2])["slowest_unit"] is None
+    units[2] = {k: nan for k in units[2]}
+    assert bench.unit_spread(units)["slowest_unit"] == 3
+    ov = bench.timeline_overlap([u for u in units if u["h2d_begin"] == u["h2d_begin"]], 10.0)
+    assert ov["step_ms"] == t + 4
