@@ -20,6 +20,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -162,8 +163,9 @@ def workload(name):
 
 # ------------------------------------------------------------ oracle ----
 
-def oracle_sample_rate(w, n_sample, steps_budget_s, max_steps, seed_offset=0):
-    """Time the oracle (single thread, as it stands) on a contiguous slice of
+def oracle_sample_rate(w, n_sample, steps_budget_s, max_steps, seed_offset=0, openmp=False):
+    """Time the oracle (single thread, as it stands; openmp=True: the same
+    source built with -fopenmp, on all host cores) on a contiguous slice of
     the workload's unit treated as a layer of its own (the clip, when on,
     is over the slice).  Inputs are generated before each timed call."""
     import numpy as np
@@ -183,10 +185,22 @@ def oracle_sample_rate(w, n_sample, steps_budget_s, max_steps, seed_offset=0):
     while steps < max_steps and (steps_budget_s <= 0 or elapsed < steps_budget_s or steps < 2):
         g = batches[steps % 2]
         t0 = time.perf_counter()
-        oracle.layer_step(g, th, m, v, wb, hp, steps + 1)
+        oracle.layer_step(g, th, m, v, wb, hp, steps + 1, openmp=openmp)
         elapsed += time.perf_counter() - t0
         steps += 1
     return n_sample * steps / elapsed / 1e9, steps, elapsed
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu; /proc/cpuinfo on x86)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.processor() or platform.machine()
 
 
 def run_reference(args):
@@ -805,13 +819,21 @@ def run_ours(args):
     value = n * K * world / (ms_total * 1e-3) / 1e9
     step_bytes = bytes_upd + bytes_pre
 
-    cpu = None
+    cpu = cpu_all = None
     if not args.no_cpu_baseline and world == 1:
         rate, steps, el = oracle_sample_rate(w, 1 << 24 if n >= (1 << 24) else n, 12.0, 1000)
         cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "gbs": rate * (26 + 2 * R), "gbs_bytes_per_param": 26 + 2 * R, "cpu_model": cpu_model(),
                "sample": f"first {min(n, 1 << 24)} parameters of the layer as a layer of their own, "
                          f"R={R}{', clip over the sample' if clip else ''}, {steps} steps "
                          f"({el:.1f} s of single-thread CPU time; inputs generated outside the timed calls)"}
+        import oracle
+        rate_all, steps_all, el_all = oracle_sample_rate(w, 1 << 24 if n >= (1 << 24) else n, 6.0, 1000,
+                                                         openmp=True)
+        cpu_all = {"value": rate_all, "unit": UNIT, "cores": oracle.threads(True), "kind": "oracle_openmp",
+                   "gbs": rate_all * (26 + 2 * R), "gbs_bytes_per_param": 26 + 2 * R, "cpu_model": cpu_model(),
+                   "sample": f"the same slice, the oracle source built with -fopenmp (element loops split "
+                             f"across threads), {steps_all} steps in {el_all:.1f} s"}
     traffic, traffic_note = None, "no ncu capture recorded for this workload"
     prof = os.path.join(ROOT, "profiles", f"traffic_{w.name}.json")
     if os.path.exists(prof):
@@ -847,6 +869,7 @@ def run_ours(args):
         "clocks": clocks,
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "cpu_baseline_all_cores": cpu_all,
         "fp32_grad_variant": variant,
         "other_hbm_workloads": others,
         "cpu_reduce_route": cpu_route,

@@ -23,8 +23,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
 _HDR = os.path.join(_HERE, "oracle.h")
 _SO = os.path.join(_HERE, "liboracle.so")
+_SO_OMP = os.path.join(_HERE, "liboracle_omp.so")
 _lock = threading.Lock()
-_lib = None
+_libs = {}
 
 
 class Hparams(C.Structure):
@@ -40,31 +41,35 @@ class StepScalars(C.Structure):
                 ("bc2_sqrt", C.c_float), ("eps", C.c_float)]
 
 
-def build(force: bool = False) -> str:
-    """Compile oracle.c into liboracle.so next to it (host C compiler)."""
+def build(force: bool = False, openmp: bool = False) -> str:
+    """Compile oracle.c into liboracle.so next to it (host C compiler).  With
+    openmp=True the same source is built with -fopenmp into liboracle_omp.so,
+    which is used only to time the oracle on all host cores."""
+    so = _SO_OMP if openmp else _SO
     with _lock:
-        fresh = os.path.exists(_SO) and all(
-            os.path.getmtime(_SO) >= os.path.getmtime(p) for p in (_SRC, _HDR))
+        fresh = os.path.exists(so) and all(
+            os.path.getmtime(so) >= os.path.getmtime(p) for p in (_SRC, _HDR))
         if fresh and not force:
-            return _SO
+            return so
         cc = os.environ.get("CC", "gcc")
-        tmp = _SO + f".tmp{os.getpid()}"
+        tmp = so + f".tmp{os.getpid()}"
         cmd = [cc, "-std=c99", "-O2", "-ffp-contract=off", "-fno-fast-math",
                "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+        if openmp:
+            cmd.insert(1, "-fopenmp")
         subprocess.run(cmd, check=True)
-        os.replace(tmp, _SO)
-        return _SO
+        os.replace(tmp, so)
+        return so
 
 
-def lib():
-    global _lib
-    if _lib is None:
+def lib(openmp: bool = False):
+    L = _libs.get(openmp)
+    if L is None:
         # ORACLE_SO lets the mutation test load a deliberately broken copy of
         # the oracle, built from an edited oracle.c in a temporary directory.
-        so = os.environ.get("ORACLE_SO")
+        so = None if openmp else os.environ.get("ORACLE_SO")
         if not so:
-            build()
-            so = _SO
+            so = build(openmp=openmp)
         L = C.CDLL(so)
         P = C.c_void_p
         L.oracle_bf16_to_f32.restype = C.c_float
@@ -94,8 +99,15 @@ def lib():
         L.oracle_layer_step_f64.restype = C.c_double
         L.oracle_layer_step_f64.argtypes = [C.c_int64, C.c_int32, P, P, P, P,
                                             C.POINTER(Hparams), C.c_int64]
-        _lib = L
-    return _lib
+        L.oracle_threads.restype = C.c_int32
+        L.oracle_threads.argtypes = []
+        _libs[openmp] = L
+    return L
+
+
+def threads(openmp: bool = False) -> int:
+    """Threads the oracle's element loops use (1 for the default build)."""
+    return lib(openmp).oracle_threads()
 
 
 def hparams(lr=1e-5, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01,
@@ -186,8 +198,9 @@ def adamw_update(gm, coef, theta, m, v, w, hp: Hparams, t: int) -> None:
                               wp, C.byref(hp), t)
 
 
-def layer_step(grads, theta, m, v, w, hp: Hparams, t: int) -> float:
-    """One step of a whole layer in place; returns the clip coefficient used."""
+def layer_step(grads, theta, m, v, w, hp: Hparams, t: int, openmp: bool = False) -> float:
+    """One step of a whole layer in place; returns the clip coefficient used.
+    openmp=True runs the -fopenmp build (all-core timing only)."""
     tab, n = _replica_table(grads)
     for a in (theta, m, v):
         _as(a, np.float32)
@@ -199,7 +212,8 @@ def layer_step(grads, theta, m, v, w, hp: Hparams, t: int) -> float:
         if w.size != n:
             raise ValueError("length mismatch")
         wp = _ptr(w)
-    fn = lib().oracle_layer_step_f32g if _is_f32(grads) else lib().oracle_layer_step
+    L = lib(openmp)
+    fn = L.oracle_layer_step_f32g if _is_f32(grads) else L.oracle_layer_step
     c = fn(n, len(grads), tab, _ptr(theta), _ptr(m), _ptr(v), wp, C.byref(hp), t)
     if c < 0:
         raise MemoryError("oracle_layer_step: allocation failed")

@@ -8,12 +8,32 @@
  * GPU library.  Build: cc -std=c99 -O2 -ffp-contract=off -fPIC -shared -lm.
  * No fast-math, no SIMD intrinsics, no threads: each FP32 operation below is
  * one IEEE-754 single-precision operation, performed in the written order.
+ *
+ * The same source also builds with -fopenmp, for one purpose only: timing the
+ * oracle on all host cores as a second CPU baseline.  Then the element loops
+ * are split across threads (each element's operations are unchanged) and the
+ * clip's double sum is taken as per-thread partials (a different summation
+ * order).  Parity tests and pins use the single-threaded build, in which the
+ * omp pragmas are ignored.
  */
 #include "oracle.h"
 
 #include <math.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* Threads the element loops use: 1 in the single-threaded build. */
+int32_t oracle_threads(void)
+{
+#ifdef _OPENMP
+    return (int32_t)omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
 
 /* ---- BF16 <-> FP32 ------------------------------------------------------
  * BF16 is the upper half of an IEEE binary32 (1 sign, 8 exponent, 7 fraction
@@ -87,6 +107,7 @@ void oracle_step_scalars_for(const oracle_hparams *hp, int64_t t, oracle_step_sc
 void oracle_grad_mean(int64_t n, int32_t R, const uint16_t *const *g, float *gm)
 {
     float fr = (float)R;
+#pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n; ++i) {
         float s = oracle_bf16_to_f32(g[0][i]);
         for (int32_t r = 1; r < R; ++r)
@@ -98,6 +119,7 @@ void oracle_grad_mean(int64_t n, int32_t R, const uint16_t *const *g, float *gm)
 void oracle_grad_mean_f32(int64_t n, int32_t R, const float *const *g, float *gm)
 {
     float fr = (float)R;
+#pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n; ++i) {
         float s = g[0][i];
         for (int32_t r = 1; r < R; ++r)
@@ -113,6 +135,7 @@ void oracle_grad_mean_f32(int64_t n, int32_t R, const float *const *g, float *gm
 double oracle_grad_sqnorm(int64_t n, const float *gm)
 {
     double s = 0.0;
+#pragma omp parallel for schedule(static) reduction(+ : s)
     for (int64_t i = 0; i < n; ++i) {
         double x = (double)gm[i];
         s = s + x * x;
@@ -151,6 +174,7 @@ void oracle_adamw_update(int64_t n, const float *gm, float coef,
 {
     oracle_step_scalars k;
     oracle_step_scalars_for(hp, t, &k);
+#pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < n; ++i) {
         float g = gm[i] * coef;
 

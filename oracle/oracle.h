@@ -107,6 +107,10 @@ float oracle_layer_step_f32g(int64_t n, int32_t R, const float *const *g,
  * corrections applied to the moments (m_hat = m/(1-b1^t), v_hat = v/(1-b2^t))
  * and the update theta = theta*(1 - lr*wd) - lr*m_hat/(sqrt(v_hat)+eps).
  * Returns the clip coefficient (1 when off), -1 on allocation failure. */
+/* Threads the element loops use (1 unless built with -fopenmp, which is for
+ * the all-core timing only). */
+int32_t oracle_threads(void);
+
 double oracle_layer_step_f64(int64_t n, int32_t R, const uint16_t *const *g,
                              double *theta, double *m, double *v,
                              const oracle_hparams *hp, int64_t t);

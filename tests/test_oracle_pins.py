@@ -414,3 +414,36 @@ def test_f32_step1_closed_form():
     gv = g.astype(np.float64)
     want = th0.astype(np.float64) * (1 - lr64 * wd64) - lr64 * gv / (np.abs(gv) + eps64)
     assert np.all(np.abs(th - want) <= 3 * ulp32(want) + lr64 * 2.0 ** -21)
+
+
+@pytest.mark.parametrize("clip", [0.0, 1.0])
+def test_openmp_build_is_the_same_oracle(clip):
+    """The -fopenmp build (used only to time the oracle on all cores) splits
+    the element loops across threads without changing any element's
+    operations: without the clip it is bit-identical to the single-threaded
+    build; with it, only the clip's double sum changes order, so the clip
+    coefficients agree to within an FP32 ulp and the states to within what
+    one ulp of the coefficient can move."""
+    rng = np.random.default_rng(7)
+    n, R = 300_001, 4
+    grads = [oracle.f32_to_bf16(rng.standard_normal(n).astype(np.float32) * 1e-3) for _ in range(R)]
+    th0 = rng.standard_normal(n).astype(np.float32) * 0.02
+    hp = oracle.hparams(max_grad_norm=clip)
+    runs = {}
+    for omp in (False, True):
+        th, m, v = th0.copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+        w = np.zeros(n, np.uint16)
+        coefs = [oracle.layer_step(grads, th, m, v, w, hp, t, openmp=omp) for t in (1, 2)]
+        runs[omp] = (coefs, th, m, v, w)
+    assert oracle.threads(False) == 1
+    assert oracle.threads(True) >= 1
+    (c0, *state0), (c1, *state1) = runs[False], runs[True]
+    if clip == 0.0:
+        assert c0 == c1 == [1.0, 1.0]
+        for a, b in zip(state0, state1):
+            assert np.array_equal(a, b)
+    else:
+        for a, b in zip(c0, c1):
+            assert abs(a - b) <= np.spacing(np.float32(a))
+        assert np.allclose(state0[0], state1[0], rtol=0, atol=1e-9)
+        assert np.allclose(state0[1], state1[1], rtol=2e-7, atol=0)
