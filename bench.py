@@ -608,6 +608,15 @@ def run_streamed(args, S, torch, synth):
         S.slide_state_destroy(st)
         del pool
     s_step = statistics.median(times)
+    cpu = None
+    if not args.no_cpu_baseline:
+        n_s = min(1 << 22, maxn)
+        rate, c_steps, c_el = oracle_sample_rate(w, n_s, 4.0, 100, seed_offset=3000)
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "s_per_step_extrapolated": N / (rate * 1e9),
+               "sample": f"first {n_s} parameters of one unit as a layer of their own, R={w.R}, "
+                         f"{c_steps} steps ({c_el:.1f} s of single-thread CPU time); the per-parameter rate "
+                         f"is extrapolated to the whole model's {N} parameters"}
     G = 1e9
     if in_hbm:   # the BF16 copy's delivery and write-back stay inside HBM
         t_roof = max(12 * N / (link["h2d_concurrent_gbs"] * G), 12 * N / (link["d2h_concurrent_gbs"] * G),
@@ -631,6 +640,7 @@ def run_streamed(args, S, torch, synth):
             "grad_callback": f"copies pre-generated replicas ({n_pool} sets, the workload's distribution) "
                              "from HBM into the window",
             "s_per_step_with_generator_callback": gen_s,
+            "cpu_baseline": cpu,
             "timeline_fastest_step": overlap_fast, "timeline_slowest_step": overlap_slow,
             "bf16_delivery": delivery,
             "timing": "host wall clock around each synchronous model step; s_per_step is the median"}
