@@ -49,9 +49,14 @@ def parse_args():
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the FP32-gradient variant, the other HBM workloads and the CPU-route legs")
     ap.add_argument("--no-streamed", action="store_true",
-                    help="skip the host-streamed leg (8-layer h=8192 model, ~98 GB pinned host memory)")
+                    help="skip the host-streamed legs (8-layer h=8192 model, ~98 GB pinned host memory; "
+                         "40-layer h=5120 model, ~177 GB pinned)")
     ap.add_argument("--streamed-workload", default="h8192x8_streamed",
-                    choices=["h8192x8_streamed", "h5120x40_streamed"])
+                    choices=["h8192x8_streamed", "h5120x40_streamed"],
+                    help="host-streamed workload of the 'streamed' key")
+    ap.add_argument("--streamed-also", default="h5120x40_streamed",
+                    help="comma-separated further host-streamed workloads, each under 'streamed_also' "
+                         "('' for none)")
     ap.add_argument("--streamed-steps", type=int, default=5)
     ap.add_argument("--streamed-bf16-in-hbm", action="store_true",
                     help="keep the BF16 copy in HBM (host holds 12 B/param); implied for h5120x40_streamed")
@@ -542,7 +547,7 @@ def measure_delivery(S, torch, st, layer, n, R, reps=3):
     return out
 
 
-def run_streamed(args, S, torch, synth):
+def run_streamed(args, S, torch, synth, name):
     """Host-resident streamed step of a whole model: s/step against the
     host-link roofline measured in the same run.  The gradient callback stands
     in for the backward pass; in the timed steps it copies pre-generated
@@ -550,11 +555,11 @@ def run_streamed(args, S, torch, synth):
     so the time is the engine's copies and update; one more step with the
     on-the-fly generator as the callback is reported beside it."""
     import ctypes as C
-    w = workload(args.streamed_workload)
+    w = workload(name)
     sizes = [u.numel for u in w.units]
     N = sum(sizes)
     maxn = max(sizes)
-    in_hbm = args.streamed_bf16_in_hbm or args.streamed_workload == "h5120x40_streamed"
+    in_hbm = args.streamed_bf16_in_hbm or name == "h5120x40_streamed"
     flags = S.SLIDE_FLAG_BF16_COPY_IN_HBM if in_hbm else 0
     _, host_b = S.slide_state_bytes(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED, flags=flags)
     need = host_b + (24 << 30)
@@ -809,9 +814,12 @@ def run_ours(args):
                                              max_steps=200 if name == "h5120_R8_logscale" else 500)
                   for name in W.HBM_RESIDENT if name != args.workload}
         cpu_route = measure_cpu_reduce_route(S, torch, synth, n, R)
-    streamed = None
+    streamed = streamed_also = None
     if not args.no_streamed and world == 1:
-        streamed = run_streamed(args, S, torch, synth)
+        streamed = run_streamed(args, S, torch, synth, args.streamed_workload)
+        also = [x for x in args.streamed_also.split(",") if x and x != args.streamed_workload]
+        if also:
+            streamed_also = {x: run_streamed(args, S, torch, synth, x) for x in also}
 
     if rank != 0:
         if dist:
@@ -884,6 +892,7 @@ def run_ours(args):
         "other_hbm_workloads": others,
         "cpu_reduce_route": cpu_route,
         "streamed": streamed,
+        "streamed_also": streamed_also,
     }
     print(json.dumps(line), flush=True)
     if dist:
