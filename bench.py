@@ -64,6 +64,9 @@ def parse_args():
                     help="copy chunk of the streamed engine (the pages' 64 MiB by default)")
     ap.add_argument("--batches", type=int, default=4,
                     help="pre-generated gradient batches cycled by the steps (1 for small profiling runs)")
+    ap.add_argument("--slice-params", type=int, default=0,
+                    help="profiling only: cut the main workload's unit to its first N parameters (the line "
+                         "then carries config.slice_params and is not a full-size measurement)")
     ap.add_argument("--soak-s", type=float, default=1.5,
                     help="seconds of untimed steps before the timed region (clocks settle, samples)")
     args = ap.parse_args()
@@ -164,6 +167,18 @@ def max_over_ranks(x: float, dist=None) -> float:
 def workload(name):
     from synth import workloads as W
     return W.ALL[name]()
+
+
+def slice_unit(unit, n):
+    """The first n parameters of a unit: its tensors in order, the last one cut."""
+    from synth import workloads as W
+    tensors, left = [], n
+    for name, k in unit.tensors:
+        if left <= 0:
+            break
+        tensors.append((name, min(k, left)))
+        left -= k
+    return W.Unit(unit.name, tensors)
 
 
 # ------------------------------------------------------------ oracle ----
@@ -283,11 +298,13 @@ def measure_hbm_workload(args, S, torch, synth, peak, w, max_steps=500):
     finally:
         S.slide_state_destroy(st)
     b_upd, b_pre = (26 + gsize * R) * n, (gsize * R * n if clip else 0)
+    traffic, traffic_note = recorded_traffic(w.name)
     return {"workload": w.name, "description": w.description, "params": n, "replicas": R, "steps": K,
             "value": n * K / (ms * 1e-3) / 1e9, "unit": UNIT, "ms_per_step": ms / K,
             "hbm_gbs": (b_upd + b_pre) / (ms / K * 1e-3) / 1e9,
             "roofline": {"bound": "hbm", "kernel": "grad_reduce_adamw_cast", "achieved": b_upd / (upd * 1e-3) / 1e9,
                          "peak": peak, "unit": "GB/s", "frac": b_upd / (upd * 1e-3) / 1e9 / peak,
+                         "traffic": traffic, "traffic_note": traffic_note, "bytes_per_launch": b_upd,
                          "bytes_per_param": 26 + gsize * R, "avg_launch_ms": upd},
             "prepass": ({"achieved": b_pre / (pre * 1e-3) / 1e9, "frac": b_pre / (pre * 1e-3) / 1e9 / peak,
                          "avg_launch_ms": pre, "bytes_per_param": gsize * R} if clip else None),
@@ -370,6 +387,21 @@ def kernel_source_sha256():
     p = os.path.join(ROOT, "mixed_precision_adam_grad_gb300", "csrc", "grad_reduce_adamw_cast.cu")
     with open(p, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()
+
+
+def recorded_traffic(name):
+    """DRAM bytes per launch of the fused kernel on a workload, from the ncu
+    summary committed under profiles/ (traffic_<workload>.json), and where
+    they come from; (None, reason) when there is none or the kernel source
+    changed since the capture."""
+    prof = os.path.join(ROOT, "profiles", f"traffic_{name}.json")
+    if not os.path.exists(prof):
+        return None, "no ncu capture recorded for this workload"
+    with open(prof) as f:
+        rec = json.load(f)
+    if rec.get("kernel_source_sha256") != kernel_source_sha256():
+        return None, "the kernel changed since the ncu capture: traffic withheld"
+    return rec.get("grad_reduce_adamw_cast_bytes_per_launch"), rec.get("source", "")
 
 
 def mem_available_bytes():
@@ -667,6 +699,8 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
     w = workload(args.workload)
+    if args.slice_params > 0:
+        w.units[0] = slice_unit(w.units[0], args.slice_params)
     n = w.units[0].numel
     R = w.R
     clip = w.max_grad_norm > 0
@@ -852,16 +886,8 @@ def run_ours(args):
                    "gbs": rate_all * (26 + 2 * R), "gbs_bytes_per_param": 26 + 2 * R, "cpu_model": cpu_model(),
                    "sample": f"the same slice, the oracle source built with -fopenmp (element loops split "
                              f"across threads), {steps_all} steps in {el_all:.1f} s"}
-    traffic, traffic_note = None, "no ncu capture recorded for this workload"
-    prof = os.path.join(ROOT, "profiles", f"traffic_{w.name}.json")
-    if os.path.exists(prof):
-        with open(prof) as f:
-            rec = json.load(f)
-        if rec.get("kernel_source_sha256") == kernel_source_sha256():
-            traffic = rec.get("grad_reduce_adamw_cast_bytes_per_launch")
-            traffic_note = rec.get("source", "")
-        else:
-            traffic_note = "the kernel changed since the ncu capture: traffic withheld"
+    traffic, traffic_note = (recorded_traffic(w.name) if args.slice_params <= 0
+                             else (None, "profiling slice: no full-launch capture applies"))
 
 
     line = {
@@ -873,7 +899,9 @@ def run_ours(args):
                    "l2": f"inputs larger than L2: each step touches {step_bytes / 1e9:.2f} GB; "
                          f"{args.batches} gradient batches cycled",
                    "clock_samples": "nvidia-smi every 200 ms over a soak of the same step and the "
-                                    "timed region"},
+                                    "timed region",
+                   **({"slice_params": n, "note": "profiling slice of the unit, not a full-size measurement"}
+                      if args.slice_params > 0 else {})},
         "hbm_gbs": step_bytes / (ms_step * 1e-3) / 1e9,
         "roofline": {"bound": "hbm", "kernel": "grad_reduce_adamw_cast",
                      "achieved": ach_upd, "peak": peak, "unit": "GB/s", "frac": ach_upd / peak,

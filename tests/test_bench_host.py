@@ -83,3 +83,14 @@ def test_unit_spread_and_overlap():
     assert bench.unit_spread(units)["slowest_unit"] == 3
     ov = bench.timeline_overlap([u for u in units if u["h2d_begin"] == u["h2d_begin"]], 10.0)
     assert ov["step_ms"] == t + 4
+
+
+def test_slice_unit_keeps_leading_tensors():
+    from synth import workloads as W
+    u = W.h5120_r8_logscale().units[0]
+    full = u.numel
+    s = bench.slice_unit(u, 100_000_000)
+    assert s.numel == 100_000_000
+    assert [t for t, _ in s.tensors] == [t for t, _ in u.tensors[:len(s.tensors)]]
+    assert all(a == b for a, b in zip(s.tensors[:-1], u.tensors))
+    assert bench.slice_unit(u, full + 5).numel == full
