@@ -54,9 +54,9 @@ def parse_args():
     ap.add_argument("--streamed-workload", default="h8192x8_streamed",
                     choices=["h8192x8_streamed", "h5120x40_streamed"],
                     help="host-streamed workload of the 'streamed' key")
-    ap.add_argument("--streamed-also", default="h5120x40_streamed",
+    ap.add_argument("--streamed-also", default="h5120x40_streamed,h8192x8_streamed+bf16hbm",
                     help="comma-separated further host-streamed workloads, each under 'streamed_also' "
-                         "('' for none)")
+                         "('' for none); a '+bf16hbm' suffix keeps the BF16 copy in HBM")
     ap.add_argument("--streamed-steps", type=int, default=5)
     ap.add_argument("--streamed-bf16-in-hbm", action="store_true",
                     help="keep the BF16 copy in HBM (host holds 12 B/param); implied for h5120x40_streamed")
@@ -579,7 +579,7 @@ def measure_delivery(S, torch, st, layer, n, R, reps=3):
     return out
 
 
-def run_streamed(args, S, torch, synth, name):
+def run_streamed(args, S, torch, synth, key):
     """Host-resident streamed step of a whole model: s/step against the
     host-link roofline measured in the same run.  The gradient callback stands
     in for the backward pass; in the timed steps it copies pre-generated
@@ -587,11 +587,14 @@ def run_streamed(args, S, torch, synth, name):
     so the time is the engine's copies and update; one more step with the
     on-the-fly generator as the callback is reported beside it."""
     import ctypes as C
+    name, _, layout = key.partition("+")
+    if layout not in ("", "bf16hbm"):
+        raise ValueError(f"unknown streamed layout suffix in {key!r}")
     w = workload(name)
     sizes = [u.numel for u in w.units]
     N = sum(sizes)
     maxn = max(sizes)
-    in_hbm = args.streamed_bf16_in_hbm or name == "h5120x40_streamed"
+    in_hbm = args.streamed_bf16_in_hbm or name == "h5120x40_streamed" or layout == "bf16hbm"
     flags = S.SLIDE_FLAG_BF16_COPY_IN_HBM if in_hbm else 0
     _, host_b = S.slide_state_bytes(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED, flags=flags)
     need = host_b + (24 << 30)
