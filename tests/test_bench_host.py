@@ -94,3 +94,10 @@ def test_slice_unit_keeps_leading_tensors():
     assert [t for t, _ in s.tensors] == [t for t, _ in u.tensors[:len(s.tensors)]]
     assert all(a == b for a, b in zip(s.tensors[:-1], u.tensors))
     assert bench.slice_unit(u, full + 5).numel == full
+
+
+def test_streamed_leg_rejects_unknown_layout_suffix():
+    class A:
+        streamed_bf16_in_hbm = False
+    with pytest.raises(ValueError):
+        bench.run_streamed(A(), None, None, None, "h8192x8_streamed+bogus")
