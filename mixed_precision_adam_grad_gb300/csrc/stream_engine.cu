@@ -52,6 +52,8 @@
 //  So the write-back of l starts while m and v of l are still arriving, the
 //  H2D engine fills the other slot with l-1 and the D2H engine drains l+1.
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
+#include <nvtx3/nvToolsExtCudaRt.h>
 
 #include <chrono>
 #include <string>
@@ -223,6 +225,12 @@ slide_status engine_create(slide_state *st)
         e = cudaStreamCreateWithFlags(&E->s_comp, cudaStreamNonBlocking);
     if (e == cudaSuccess)
         e = cudaStreamCreateWithFlags(&E->s_d2h, cudaStreamNonBlocking);
+    if (e == cudaSuccess) {
+        // names for a profiler's timeline (no effect without one attached)
+        nvtxNameCudaStreamA(E->s_h2d, "slide host-to-device");
+        nvtxNameCudaStreamA(E->s_comp, "slide update");
+        nvtxNameCudaStreamA(E->s_d2h, "slide device-to-host");
+    }
     if (e != cudaSuccess) {
         slide_status rc = fail_cuda(e, "streaming engine set-up");
         destroy_engine_objects(E);
@@ -285,6 +293,12 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
 
     for (int l = 0; l < L; ++l)
         E->recorded[l] = 0;
+    // Profiler ranges (host side: when each part was enqueued): the step, and
+    // each unit of the reverse sweep.  No effect without a profiler attached.
+    struct Range {
+        explicit Range(const std::string &name) { nvtxRangePushA(name.c_str()); }
+        ~Range() { nvtxRangePop(); }
+    } step_range("slide streamed step t=" + std::to_string(t));
     e = cudaEventRecord(E->step_start, E->s_h2d);
 
     // forward sweep: deliver the BF16 copy of every unit, in order (a copy
@@ -344,6 +358,7 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
         Slot &s = E->slots[l % kSlots];
         LayerState &U = st->layers[l];
         const int K = E->n_chunks(U.n);
+        Range unit_range("slide unit " + std::to_string(l) + " (slot " + std::to_string(l % kSlots) + ")");
         // prefetch the next unit of the sweep into the other slot
         if (l > 0) {
             e = copy_in(l - 1);
