@@ -100,8 +100,10 @@ enum {
     SLIDE_FLAG_BF16_COPY_IN_HBM = 8u     /* streamed residency: keep the BF16 compute copy in HBM
                                             (2 B/param of device memory) instead of the pinned host
                                             mirror; the host holds 12 B/param and the link carries
-                                            12 B/param each way per step (the delivery and the
-                                            write-back of the BF16 copy stay inside HBM) */
+                                            12 B/param each way per step (the update writes each
+                                            unit's resident copy in place: the copy is neither
+                                            delivered nor written back, and the window has no BF16
+                                            buffers) */
 };
 
 /* Adam hyper-parameters (FP32).  Valid: lr >= 0, 0 <= beta1 < 1,
