@@ -33,6 +33,9 @@ def test_c_client_host_calls(tmp_path):
 
 @pytest.mark.gpu
 def test_c_client_gpu_step(tmp_path):
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
     exe = _build(tmp_path)
     r = subprocess.run([exe, "gpu"], capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stdout + r.stderr
