@@ -1,19 +1,24 @@
 #!/usr/bin/env python3
 """Benchmark of the per-layer mixed-precision AdamW step on GB300.
 
-Workload (default): one h=2560 decoder layer (100,930,560 parameters), R = 4
-BF16 gradient replicas averaged in the kernel, global grad-norm clip at 1.0,
-lr 1e-5, betas 0.9/0.999, eps 1e-8, weight decay 0.01.  A step is one
-slide_layer_step: the clip pre-pass plus the fused
-grad_reduce_adamw_cast kernel over one batch of R synthetic replicas (four
-pre-generated batches are cycled; every step touches ~4.2 GB, far more than
-the 129 MB L2).  The warm-up steps play the workload's pre-warm of m and v.
+Workload of the headline (default): one h=5120 decoder layer (330,311,680
+parameters), R = 8 BF16 gradient replicas averaged in the kernel, per-tensor
+gradient scales drawn log-uniform in [1e-5, 1e-2], lr 1e-5, betas
+0.9/0.999, eps 1e-8, weight decay 0.01.  This is the largest HBM-resident
+workload.  A step is one slide_layer_step: the fused grad_reduce_adamw_cast
+kernel (plus the clip pre-pass when the workload clips) over one batch of R
+synthetic replicas (pre-generated batches are cycled; every step touches
+13.9 GB, far more than the 129 MB L2).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-Prints one JSON line (rank 0).  Under torchrun each rank updates its own
-layer (independent problems, no collective on the data path: weak scaling);
-the value is all ranks' parameters over the slowest rank's time.
+Output: detail lines (one per leg, prefixed "detail ") and, LAST, one compact
+JSON line (under 4 KB) with the headline, the roofline, the baselines, the
+end-to-end figure and a short summary of every other leg.  --detail-out PATH
+also writes the whole record as one JSON file.  Under torchrun each rank
+updates its own layer (independent problems, no collective on the data path:
+weak scaling); the value is all ranks' parameters over the slowest rank's
+time.
 """
 from __future__ import annotations
 
@@ -41,8 +46,11 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="h2560_R4_clip", choices=["h2560_R1", "h2560_R4_clip", "h5120_R8_logscale"],
-                    help="HBM-resident workload of the main line")
+    ap.add_argument("--workload", default="h5120_R8_logscale",
+                    choices=["h2560_R1", "h2560_R4_clip", "h5120_R8_logscale"],
+                    help="HBM-resident workload of the headline")
+    ap.add_argument("--detail-out", default="",
+                    help="also write the whole record (every leg in full) to this JSON file")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=100)
@@ -305,79 +313,10 @@ def measure_hbm_workload(args, S, torch, synth, peak, w, max_steps=500):
             "roofline": {"bound": "hbm", "kernel": "grad_reduce_adamw_cast", "achieved": b_upd / (upd * 1e-3) / 1e9,
                          "peak": peak, "unit": "GB/s", "frac": b_upd / (upd * 1e-3) / 1e9 / peak,
                          "traffic": traffic, "traffic_note": traffic_note, "bytes_per_launch": b_upd,
-                         "bytes_per_param": 26 + gsize * R, "avg_launch_ms": upd},
+                         "bytes_per_param": 26 + gsize * R, "avg_launch_ms": upd, "launches": K},
             "prepass": ({"achieved": b_pre / (pre * 1e-3) / 1e9, "frac": b_pre / (pre * 1e-3) / 1e9 / peak,
                          "avg_launch_ms": pre, "bytes_per_param": gsize * R} if clip else None),
             "step_roofline_frac": (b_upd + b_pre) / (ms / K * 1e-3) / 1e9 / peak}
-
-
-# ---------------------------------------------------- CPU-reduce route ----
-
-def host_replica_mean(reps_bf16):
-    """Mean of R BF16 replicas on the host: widen, FP32 sum in replica order,
-    divide by R (the reduction the CPU route performs)."""
-    import numpy as np
-    acc = (reps_bf16[0].astype(np.uint32) << 16).view(np.float32).copy()
-    for g in reps_bf16[1:]:
-        acc += (g.astype(np.uint32) << 16).view(np.float32)
-    acc /= np.float32(len(reps_bf16))
-    return acc
-
-
-def measure_cpu_reduce_route(S, torch, synth, n, R, seed=1, hp=None):
-    """The CPU-reduce route of the pages (every replica leaves the GPU and is
-    reduced on the host: R x 2n bytes device->host) against the GPU route
-    (the replicas are averaged inside the update kernel and never leave HBM).
-    The host mean returns to the GPU as one FP32 replica (4n bytes), so both
-    routes must produce bit-identical states; that is checked."""
-    import numpy as np
-    hp = hp or S.hparams(max_grad_norm=1.0)
-    sp = synth.spec(seed)
-    reps = [torch.empty(n + 64, dtype=torch.int16, device="cuda") for _ in range(R)]
-    for r in range(R):
-        synth.dev_grad(reps[r].data_ptr(), n, sp, 0, 1, r, 1e-3)
-    th0 = synth.master(n, seed)
-    gpu = S.slide_state_create([n], R)
-    cpu = S.slide_state_create([n], 1, flags=S.SLIDE_FLAG_FP32_GRADS)
-    host_reps = [torch.empty(n, dtype=torch.int16, pin_memory=True) for _ in range(R)]
-    mean_host = torch.empty(n, dtype=torch.float32, pin_memory=True)
-    mean_dev = torch.empty(n + 64, dtype=torch.float32, device="cuda")
-    try:
-        S.slide_layer_set(gpu, 0, master=th0, step=0)
-        S.slide_layer_set(cpu, 0, master=th0, step=0)
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        S.slide_layer_step(gpu, 0, reps, hp)
-        torch.cuda.synchronize()
-        t_gpu = time.perf_counter() - t0
-        t0 = time.perf_counter()
-        for r in range(R):
-            host_reps[r].copy_(reps[r][:n], non_blocking=True)
-        torch.cuda.synchronize()
-        t_d2h = time.perf_counter() - t0
-        t0 = time.perf_counter()
-        mean = host_replica_mean([h.numpy().view(np.uint16) for h in host_reps])
-        t_reduce = time.perf_counter() - t0
-        t0 = time.perf_counter()
-        mean_host.numpy()[:] = mean
-        mean_dev[:n].copy_(mean_host, non_blocking=True)
-        S.slide_layer_step(cpu, 0, [mean_dev], hp)
-        torch.cuda.synchronize()
-        t_back = time.perf_counter() - t0
-        a = [np.empty(n, np.float32) for _ in range(3)] + [np.empty(n, np.uint16)]
-        b = [np.empty(n, np.float32) for _ in range(3)] + [np.empty(n, np.uint16)]
-        S.slide_layer_get(gpu, 0, *a)
-        S.slide_layer_get(cpu, 0, *b)
-        same = all(np.array_equal(x.view(np.uint8), y.view(np.uint8)) for x, y in zip(a, b))
-    finally:
-        S.slide_state_destroy(gpu)
-        S.slide_state_destroy(cpu)
-    return {"params": n, "replicas": R, "identical_results": bool(same),
-            "gpu_route": {"s": t_gpu, "link_bytes": 0},
-            "cpu_route": {"s": t_d2h + t_reduce + t_back, "d2h_s": t_d2h, "host_reduce_s": t_reduce,
-                          "h2d_and_update_s": t_back, "link_bytes": R * 2 * n + 4 * n,
-                          "host_reduce": "numpy FP32 in replica order, one host thread"},
-            "amplification_d2h_bytes": f"{R} x 2n (every replica) instead of none"}
 
 
 # ----------------------------------------------------------- streamed ----
@@ -850,7 +789,8 @@ def run_ours(args):
         others = {name: measure_hbm_workload(args, S, torch, synth, peak0, W.ALL[name](),
                                              max_steps=200 if name == "h5120_R8_logscale" else 500)
                   for name in W.HBM_RESIDENT if name != args.workload}
-        cpu_route = measure_cpu_reduce_route(S, torch, synth, n, R)
+        import reduce_routes
+        cpu_route = reduce_routes.measure_cpu_reduce_route(S, torch, synth, n, R)
     streamed = streamed_also = None
     if not args.no_streamed and world == 1:
         streamed = run_streamed(args, S, torch, synth, args.streamed_workload)
@@ -910,7 +850,7 @@ def run_ours(args):
                      "achieved": ach_upd, "peak": peak, "unit": "GB/s", "frac": ach_upd / peak,
                      "traffic": traffic, "traffic_note": traffic_note, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                      "bytes_per_launch": bytes_upd, "avg_launch_ms": upd_avg,
-                     "bytes_per_param": 26 + 2 * R},
+                     "bytes_per_param": 26 + 2 * R, "launches": K},
         "prepass": ({"kernel": "grad_sqnorm", "achieved": ach_pre, "unit": "GB/s", "frac": ach_pre / peak,
                      "bytes_per_launch": bytes_pre, "avg_launch_ms": pre_avg} if clip else None),
         "step_roofline_frac": (step_bytes / (ms_step * 1e-3) / 1e9) / peak,
@@ -925,10 +865,139 @@ def run_ours(args):
         "streamed": streamed,
         "streamed_also": streamed_also,
     }
-    print(json.dumps(line), flush=True)
+    report(line, args.detail_out)
     if dist:
         dist.destroy_process_group()
     return 0
+
+
+# ------------------------------------------------------------- report ----
+
+def _r(x, digits=4):
+    """x rounded to `digits` significant digits (None and non-floats as is)."""
+    if isinstance(x, float):
+        if x != x or x in (float("inf"), float("-inf")):
+            return None
+        return float(f"{x:.{digits}g}")
+    return x
+
+
+def _pick(d, keys):
+    return {k: _r(d[k]) for k in keys if d is not None and k in d and d[k] is not None}
+
+
+def compact_hbm_leg(leg):
+    """One HBM-resident leg in a few fields: rate, kernel and step fractions."""
+    if leg is None:
+        return None
+    out = {"value": _r(leg["value"]), "frac": _r(leg["roofline"]["frac"]),
+           "step_frac": _r(leg["step_roofline_frac"]), "launches": leg["steps"]}
+    if leg.get("prepass"):
+        out["prepass_frac"] = _r(leg["prepass"]["frac"])
+    return out
+
+
+def compact_streamed(leg):
+    """One host-streamed leg: median s/step against the link roofline, the
+    concurrent link rates it was measured against and the unit spread (median
+    over the steps, and the worst step)."""
+    if leg is None:
+        return None
+    if "skipped" in leg:
+        return {"skipped": leg["skipped"][:160]}
+    spreads = sorted(p["unit_max_over_median"] for p in leg.get("per_step", [])
+                     if p.get("unit_max_over_median") is not None)
+    link = leg.get("link", {})
+    out = {"bf16_in_hbm": leg["bf16_copy_in_hbm"], "s_per_step": _r(leg["s_per_step"]),
+           "roofline_s": _r(leg["roofline_s"]), "frac": _r(leg["frac"]),
+           "frac_fastest": _r(leg["frac_fastest_step"]),
+           "link_gbs_each_way": _r(leg["achieved_link_gbs_each_way"]),
+           "link_concurrent_gbs": [_r(link.get("h2d_concurrent_gbs"), 3), _r(link.get("d2h_concurrent_gbs"), 3)],
+           "unit_max_over_median": _r(statistics.median(spreads), 3) if spreads else None,
+           "unit_max_over_median_worst": _r(spreads[-1], 3) if spreads else None,
+           "chunk_mib": [leg.get("chunk_h2d_mib", leg.get("chunk_mib")), leg.get("chunk_d2h_mib", leg.get("chunk_mib"))]}
+    if "pinned_arena" in leg:
+        out["pinned_arena"] = leg["pinned_arena"]
+    if leg.get("cpu_baseline"):
+        out["cpu_s_per_step"] = _r(leg["cpu_baseline"]["s_per_step_extrapolated"], 3)
+    return out
+
+
+HEADLINE_KEYS = ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                 "scaling", "vs_baseline", "dtype", "data")
+
+
+def compact_headline(full):
+    """The last stdout line: the headline workload and the roofline of its
+    dominant kernel, the CPU baselines, the end-to-end figure, the clocks and
+    one short summary per other leg; the timelines, per-step arrays and link
+    monitors stay in the detail lines."""
+    line = {k: _r(full[k]) for k in HEADLINE_KEYS}
+    cfg = full["config"]
+    line["config"] = {k: cfg[k] for k in ("workload", "description", "params", "replicas", "max_grad_norm",
+                                          "parallelism", "l2") if k in cfg}
+    if "slice_params" in cfg:
+        line["config"]["slice_params"] = cfg["slice_params"]
+    rf = full["roofline"]
+    line["roofline"] = {k: _r(rf[k]) for k in ("bound", "kernel", "achieved", "peak", "unit", "frac", "traffic",
+                                               "bytes_per_launch", "bytes_per_param", "avg_launch_ms",
+                                               "launches")}
+    line["roofline"]["peak_kind"] = "measured" if rf.get("peak_kind", "").startswith("measured") else "fallback"
+    line["hbm_gbs"] = _r(full["hbm_gbs"])
+    line["step_roofline_frac"] = _r(full["step_roofline_frac"])
+    if full.get("prepass"):
+        line["prepass"] = _pick(full["prepass"], ("kernel", "achieved", "frac", "avg_launch_ms"))
+    line["gpu_launches"] = full["gpu_launches"]
+    ck = full.get("clocks") or {}
+    line["clocks"] = {"sm_mhz": ck.get("sm_mhz"), "sm_max_mhz": ck.get("sm_max_mhz"),
+                      "reasons": ck.get("reasons", []), "samples": ck.get("samples")}
+    if full.get("e2e"):
+        line["e2e"] = _pick(full["e2e"], ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step", "steps"))
+    for k in ("cpu_baseline", "cpu_baseline_all_cores"):
+        c = full.get(k)
+        if c:
+            line[k] = {"value": _r(c["value"]), "unit": c["unit"], "cores": c["cores"], "kind": c["kind"],
+                       "gbs": _r(c.get("gbs")), "sample": c["sample"][:160]}
+    legs = {}
+    for name, leg in (full.get("other_hbm_workloads") or {}).items():
+        legs[name] = compact_hbm_leg(leg)
+    if full.get("fp32_grad_variant"):
+        legs[full["fp32_grad_variant"]["workload"]] = compact_hbm_leg(full["fp32_grad_variant"])
+    if legs:
+        line["hbm_legs"] = legs
+    st = {}
+    if full.get("streamed"):
+        st[full["streamed"]["workload"] + ("+bf16hbm" if full["streamed"].get("bf16_copy_in_hbm") else "")] = \
+            compact_streamed(full["streamed"])
+    for name, leg in (full.get("streamed_also") or {}).items():
+        st[name] = compact_streamed(leg)
+    if st:
+        line["streamed"] = st
+    cr = full.get("cpu_reduce_route")
+    if cr:
+        line["cpu_reduce_route"] = {"cpu_route_s": _r(cr["cpu_route"]["s"]), "gpu_route_s": _r(cr["gpu_route"]["s"]),
+                                    "cpu_route_d2h_bytes": cr["cpu_route"]["d2h_bytes"],
+                                    "identical_results": cr["identical_results"]}
+    sw = full.get("chunk_sweep")
+    if sw:
+        line["chunk_sweep"] = {"workload": sw["workload"], "chosen": sw.get("chosen"),
+                               "points": [[p["h2d_mib"], p["d2h_mib"], _r(p["frac"])] for p in sw["points"]]}
+    return line
+
+
+def report(full, detail_out=""):
+    """Print every leg in full on its own "detail" line, then the compact
+    headline as the last line of stdout; optionally write the whole record."""
+    for key in ("other_hbm_workloads", "fp32_grad_variant", "cpu_reduce_route", "chunk_sweep", "streamed",
+                "streamed_also"):
+        if full.get(key) is not None:
+            print("detail " + json.dumps({key: full[key]}), flush=True)
+    if detail_out:
+        with open(detail_out, "w") as f:
+            json.dump(full, f, indent=1)
+    line = compact_headline(full)
+    print(json.dumps(line, separators=(",", ":")), flush=True)
+    return line
 
 
 def main():

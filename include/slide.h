@@ -142,15 +142,28 @@ typedef int (*slide_grad_fn)(void *user, int32_t layer, void *const *replica_dev
 /* Create a state: allocates master, m, v, the BF16 copy (all zero, t = 0) and
  * the per-layer device scratch of the clip reduction; for the streamed
  * residency also the pinned host state, the 2-slot HBM window and the copy
- * and compute streams.  *out is set only on SLIDE_OK. */
+ * and compute streams.  *out is set only on SLIDE_OK.
+ * Defined by: "SlideDP: Scaling Host-Resident LLM Fine-Tuning Across Multiple
+ * GPUs", Prerequisites (the 16N-byte state of mixed-precision Adam) and Core
+ * method (one authoritative FP32 master and (m_l, v_l) per layer, held on the
+ * host; a bounded, reusable BF16 window per GPU); "An Efficient Heterogeneous
+ * Co-Design for Fine-Tuning on a Single GPU", section 2.2 (the window
+ * pre-allocated once, of fixed size). */
 SLIDE_API slide_status slide_state_create(const slide_config *cfg, slide_state **out);
 
 /* Free everything the state owns after waiting for its own streams.
- * NULL-safe.  Work the caller enqueued on its own streams must be done. */
+ * NULL-safe.  Work the caller enqueued on its own streams must be done.
+ * Defined by: the same passages as slide_state_create (the state owns all of
+ * its memory). */
 SLIDE_API void slide_state_destroy(slide_state *st);
 
 /* Bytes slide_state_create would allocate for cfg, computed on the host
- * without touching a GPU: device (HBM) bytes and pinned host bytes. */
+ * without touching a GPU: device (HBM) bytes and pinned host bytes.
+ * Defined by: "SlideDP: Scaling Host-Resident LLM Fine-Tuning Across Multiple
+ * GPUs", Prerequisites (16N bytes = 2N + 2N + 4N + 8N); "Accelerating the
+ * Training of Large Language Models using Efficient Activation
+ * Rematerialization and Optimal Hybrid Parallelism", section 3 (12 bytes of
+ * FP32 master and Adam state per parameter). */
 SLIDE_API slide_status slide_state_bytes(const slide_config *cfg, int64_t *device_bytes,
                                int64_t *host_pinned_bytes);
 
@@ -164,7 +177,13 @@ SLIDE_API slide_status slide_state_bytes(const slide_config *cfg, int64_t *devic
  *   bf16_out: device pointer receiving the BF16 copy, or NULL for the state's
  *     own copy (slide_layer_ptrs).  16-byte aligned.
  * Stream-ordered: returns before the GPU finishes.  Steps of one layer must be
- * ordered with each other (same stream, or synchronised by the caller). */
+ * ordered with each other (same stream, or synchronised by the caller).
+ * Defined by: "SlideDP: Scaling Host-Resident LLM Fine-Tuning Across Multiple
+ * GPUs", Core method (the R ranks' gradients of a layer reduced on the GPU;
+ * one aggregated Adam update of the layer's FP32 master and moments per
+ * iteration, LayerAdam; the result cast FP32 -> BF16 for the next delivery)
+ * and Method steps (backward -> reduce -> transfer -> Adam, layer by layer).
+ * The clip is the workload's; the pages describe none. */
 SLIDE_API slide_status slide_layer_step(slide_state *st, int32_t layer, const void *const *grad_replicas,
                               const slide_adam_hparams *hp, slide_stream_t stream, void *bf16_out);
 
@@ -185,31 +204,51 @@ SLIDE_API slide_status slide_layer_step(slide_state *st, int32_t layer, const vo
  * last write-back is complete.  If fn fails or a wait times out the sweep
  * stops: units already written back carry t+1, the rest t, the state is marked
  * aborted and every later step returns SLIDE_ERR_ABORTED until slide_layer_set
- * has restored a common version on all units. */
+ * has restored a common version on all units.
+ * Defined by: "SlideDP: Scaling Host-Resident LLM Fine-Tuning Across Multiple
+ * GPUs", Core method (the chunked copy pipeline with 64 MiB chunks, the update
+ * of a chunk released as soon as it has landed) and Method steps (the version
+ * gate: a layer's next delivery waits for its update; one update per layer
+ * per iteration); "An Efficient Heterogeneous Co-Design for Fine-Tuning on a
+ * Single GPU", section 2.1 (layer-granular sliding window: prefetch of the
+ * next layer while the current one computes, asynchronous update);
+ * "Accelerating the Training of Large Language Models using Efficient
+ * Activation Rematerialization and Optimal Hybrid Parallelism", section 5.1
+ * (event-serialised copies on their own streams, ping-pong buffers, pinned
+ * host memory). */
 SLIDE_API slide_status slide_model_step_streamed(slide_state *st, slide_grad_fn fn, void *user,
                                        const slide_adam_hparams *hp);
 
 /* Copy host arrays into a layer's master / m / v (any may be NULL: left
  * unchanged) and set its step count t (>= 0).  Also rewrites the BF16 copy as
  * bf16(master) when master is given.  Synchronous.  Clears the aborted mark
- * once all units share one t. */
+ * once all units share one t.
+ * Defined by: "SlideDP: Scaling Host-Resident LLM Fine-Tuning Across Multiple
+ * GPUs", Core method (the per-layer FP32 master and moments that this call
+ * restores, for checkpoints and pre-warm hand-off) and Method steps (the
+ * version gate that the common t re-establishes). */
 SLIDE_API slide_status slide_layer_set(slide_state *st, int32_t layer, const float *master, const float *m,
                              const float *v, int64_t step);
 
 /* Copy a layer's master / m / v / BF16 copy into host arrays (any may be NULL)
- * and report t.  Synchronous: waits for the state's and the device's work. */
+ * and report t.  Synchronous: waits for the state's and the device's work.
+ * Defined by: the same passages as slide_layer_set (reading the state back). */
 SLIDE_API slide_status slide_layer_get(slide_state *st, int32_t layer, float *master, float *m, float *v,
                              uint16_t *bf16, int64_t *step);
 
 /* Where a layer's arrays live: device pointers for the HBM residency; for the
  * streamed one pinned host pointers (also addressable by kernels through the
  * unified address space), except the BF16 copy, which is a device pointer
- * with SLIDE_FLAG_BF16_COPY_IN_HBM.  Owned by the state, valid until destroy. */
+ * with SLIDE_FLAG_BF16_COPY_IN_HBM.  Owned by the state, valid until destroy.
+ * Defined by: "SlideDP: Scaling Host-Resident LLM Fine-Tuning Across Multiple
+ * GPUs", Prerequisites and Core method (where the 16N-byte state lives). */
 SLIDE_API slide_status slide_layer_ptrs(slide_state *st, int32_t layer, float **master, float **m, float **v,
                               uint16_t **bf16);
 
 /* Clip coefficient used by the last slide_layer_step of `layer` that had the
- * clip on (copied from the device; synchronous).  1.0 before any such step. */
+ * clip on (copied from the device; synchronous).  1.0 before any such step.
+ * Defined by: the global grad-norm clip of the workload; no passage of the
+ * pages describes a clip (see slide_layer_step). */
 SLIDE_API slide_status slide_layer_last_clip_coef(slide_state *st, int32_t layer, float *coef);
 
 /* Status of the steps of `layer` since the previous call (HBM residency):
@@ -220,43 +259,69 @@ SLIDE_API slide_status slide_layer_last_clip_coef(slide_state *st, int32_t layer
  *   SLIDE_ERR_NONFINITE with SLIDE_FLAG_CHECK_FINITE, if a mean gradient held
  *                       a NaN or Inf (the update was applied: the caller
  *                       decides, for example to restore with slide_layer_set);
- *   SLIDE_OK            otherwise. */
+ *   SLIDE_OK            otherwise.
+ * Defined by: "SlideDP: Scaling Host-Resident LLM Fine-Tuning Across Multiple
+ * GPUs", Method steps (a layer is delivered again only after its update is
+ * complete: this call tells the caller that an update did not complete). */
 SLIDE_API slide_status slide_layer_status(slide_state *st, int32_t layer);
 
 /* Tracing: CUDA events (cudaEvent_t values, created by the caller) that every
  * following slide_layer_step of this state records on its stream: before the
  * clip pre-pass, before the fused kernel and after it (any may be NULL; all
  * NULL turns tracing off).  Recording adds no synchronisation.  The caller may
- * pass fresh events before each step to time every launch separately. */
+ * pass fresh events before each step to time every launch separately.
+ * Defined by: "SlideDP: Scaling Host-Resident LLM Fine-Tuning Across Multiple
+ * GPUs", Reproduction (per-phase timing of the step with GPU events). */
 SLIDE_API slide_status slide_trace_events(slide_state *st, void *ev_prepass_start,
                                           void *ev_update_start, void *ev_update_stop);
 
 /* The fused step for callers that cannot allocate GPU memory.  The paper has
- * no counterpart to this entry point; it exists for code that may not call
- * cudaMalloc (an allocator hook or host callback that must not re-enter the
- * CUDA allocator, a process whose GPU memory pool is owned and capped by a
- * framework, a runtime that forbids allocation after start-up) and so cannot
- * hold a slide_state.
+ * no counterpart to this entry point.  It serves code that may not call
+ * cudaMalloc or anything that allocates device memory: an allocator hook or
+ * memory-pressure handler that must not re-enter the CUDA allocator it is part
+ * of, a process whose GPU memory is a pool owned and capped by a framework (an
+ * allocation beside the pool can fail or break its accounting), or a runtime
+ * that forbids allocation after start-up.  Such code cannot hold a
+ * slide_state, which owns its memory.
  *   The caller owns every array: grad_replicas (host array of n_replicas
  *   device pointers to n BF16 values each), master, m, v (n FP32 values each,
  *   updated in place) and bf16_out (n BF16 values written); all device
  *   pointers, 16-byte aligned.  step is the 1-based update count t of this
  *   update (the caller keeps it).  Same arithmetic as slide_layer_step.
- *   The clip's scratch (4096 per-block partial sums and the coefficient,
- *   about 32 KiB) is a fixed array in the library's device memory, allocated
- *   when the library is loaded on a GPU and held until the process exits; the
- *   call allocates and frees nothing.  Limits: 0 <= n <= 2^40 and
- *   1 <= n_replicas <= 8; anything else returns SLIDE_ERR_INVALID_ARG.
- *   The first call on a device (with that device current) looks up the
- *   scratch's device address with cudaGetSymbolAddress and caches it; make
- *   that first call before any stream capture.  Every call shares the one
- *   scratch, so calls that may overlap on the GPU (different streams, not
- *   ordered) race with each other: order them.  Stream-ordered; returns before
- *   the GPU finishes. */
+ *   The clip's scratch (4096 per-block partial sums, the coefficient and a
+ *   status word, about 32 KiB) is one fixed array in the library's device
+ *   memory; every GPU that loads the library holds it until the process
+ *   exits.  Limits: 0 <= n <= 2^40 and 1 <= n_replicas <= 8; anything else
+ *   returns SLIDE_ERR_INVALID_ARG.
+ *   Set-up: the first call on a device (with that device current) looks up
+ *   the scratch's device address with cudaGetSymbolAddress and loads every
+ *   kernel this entry point can launch.  On a context that loads device code
+ *   lazily (the CUDA default) that first call may therefore load the
+ *   library's code and allocate its static memory: make it at start-up, and
+ *   before any stream capture.  Later calls allocate and free nothing.
+ *   Sharing: every call on a device uses the one scratch, and each call
+ *   overwrites what the previous one left there (the pre-pass rewrites every
+ *   partial sum the update then reads, so nothing needs clearing).  Calls that
+ *   may overlap on the GPU (different streams, not ordered) race with each
+ *   other: order them.
+ *   Errors: argument errors are returned before anything is enqueued.  A
+ *   bounded wait inside the update kernel that runs out (2 s) leaves that
+ *   step incomplete and marks the shared status word, which
+ *   slide_noalloc_status reads.  Stream-ordered; returns before the GPU
+ *   finishes. */
 SLIDE_API slide_status slide_adamw_step_noalloc(int64_t n, int32_t n_replicas, const void *const *grad_replicas,
                                                 float *master, float *m, float *v, void *bf16_out,
                                                 const slide_adam_hparams *hp, int64_t step,
                                                 slide_stream_t stream);
+
+/* Status of the slide_adamw_step_noalloc calls on the current device since the
+ * previous slide_noalloc_status: waits for `stream`, reads and clears the
+ * shared status word (no allocation), and returns SLIDE_ERR_TIMEOUT if a
+ * bounded wait inside the update kernel ran out (that step is incomplete: the
+ * caller restores its arrays), else SLIDE_OK.  The paper has no counterpart:
+ * it completes slide_adamw_step_noalloc, whose calls have no state to hold a
+ * status. */
+SLIDE_API slide_status slide_noalloc_status(slide_stream_t stream);
 
 enum {
     SLIDE_DELIVER_FULL = 0,    /* every consumer receives the whole copy from the source */
@@ -277,7 +342,8 @@ enum {
  * sharded delivery plus GPU all-gather.
  *   dst: host array of n_consumers device pointers (16-byte aligned), each to
  *   layer_numel[layer] BF16 values; n_consumers in [1, 8].  Stream-ordered on
- *   `stream`; the source must not be updated until the delivery has run. */
+ *   `stream`; the source must not be updated until the delivery has run.
+ * Defined by: the passage cited above. */
 SLIDE_API slide_status slide_deliver_bf16(slide_state *st, int32_t layer, void *const *dst, int32_t n_consumers,
                                           int32_t route, slide_stream_t stream);
 
@@ -288,13 +354,18 @@ SLIDE_API slide_status slide_deliver_bf16(slide_state *st, int32_t layer, void *
  *   [6l+2] copy-in ended                 [6l+3] update kernel ended
  *   [6l+4] write-back began              [6l+5] write-back ended
  * and out[6L] = end of the forward sweep (BF16 delivery); NaN where a unit
- * did not get that far.  cap = number of doubles in out (>= 6L + 1). */
+ * did not get that far.  cap = number of doubles in out (>= 6L + 1).
+ * Defined by: "SlideDP: Scaling Host-Resident LLM Fine-Tuning Across Multiple
+ * GPUs", Core method and its figure on the chunked pipeline (how the copies
+ * in, the update and the copies out of a layer overlap). */
 SLIDE_API slide_status slide_streamed_timeline(slide_state *st, double *out, int64_t cap);
 
-/* Message of the last error on this host thread ("" if none). */
+/* Message of the last error on this host thread ("" if none).
+ * Defined by: no passage; error reporting of this C ABI. */
 SLIDE_API const char *slide_last_error(void);
 
-/* SLIDE_ABI_VERSION of the loaded library. */
+/* SLIDE_ABI_VERSION of the loaded library.
+ * Defined by: no passage; versioning of this C ABI. */
 SLIDE_API int32_t slide_abi_version(void);
 
 #ifdef __cplusplus

@@ -11,7 +11,7 @@ from ._binding import (SlideError, SlideState, hparams, LIB_PATH,  # noqa: F401
                        slide_state_create, slide_state_destroy, slide_layer_step,
                        slide_model_step_streamed, slide_layer_set, slide_layer_get,
                        slide_layer_ptrs, slide_layer_last_clip_coef, slide_layer_status,
-                       slide_trace_events, slide_adamw_step_noalloc,
+                       slide_trace_events, slide_adamw_step_noalloc, slide_noalloc_status,
                        slide_streamed_timeline, slide_deliver_bf16)
 
 

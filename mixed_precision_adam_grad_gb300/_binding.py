@@ -99,6 +99,8 @@ def _load():
     L.slide_adamw_step_noalloc.argtypes = [C.c_int64, C.c_int32, C.POINTER(C.c_void_p), P, P, P, P,
                                            C.POINTER(slide_adam_hparams), C.c_int64, P]
     L.slide_adamw_step_noalloc.restype = S
+    L.slide_noalloc_status.argtypes = [P]
+    L.slide_noalloc_status.restype = S
     L.slide_last_error.argtypes = []
     L.slide_last_error.restype = C.c_char_p
     L.slide_abi_version.argtypes = []
@@ -282,11 +284,21 @@ def slide_trace_events(st: SlideState, prepass_start=None, update_start=None, up
 def slide_adamw_step_noalloc(n: int, grad_replicas, master, m, v, bf16_out, hp: slide_adam_hparams,
                              step: int, stream=None) -> None:
     """The step for callers that cannot allocate GPU memory: the caller owns
-    every array and the 1-based step count; the library allocates nothing."""
+    every array and the 1-based step count; after the first call on a device
+    (its one-time set-up) the library allocates nothing."""
     ptrs = [_ptr(g) for g in grad_replicas]
     arr = (C.c_void_p * max(1, len(ptrs)))(*ptrs)
     _check(_lib().slide_adamw_step_noalloc(n, len(ptrs), arr, _ptr(master), _ptr(m), _ptr(v), _ptr(bf16_out),
                                            C.byref(hp), step, _stream(stream)))
+
+
+def slide_noalloc_status(stream=None) -> int:
+    """Status of the no-alloc calls on the current device since the last
+    query (SLIDE_OK or SLIDE_ERR_TIMEOUT); raises on other errors."""
+    rc = _lib().slide_noalloc_status(_stream(stream))
+    if rc not in (SLIDE_OK, SLIDE_ERR_TIMEOUT):
+        _check(rc)
+    return rc
 
 
 def slide_streamed_timeline(st: SlideState):

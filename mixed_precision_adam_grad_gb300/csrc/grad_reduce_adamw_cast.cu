@@ -46,6 +46,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "slide_kernels.h"
 
 namespace slide {
@@ -569,34 +571,39 @@ __global__ void __launch_bounds__(kThreads) k_grad_sqnorm(SqArgs a)
     }
 }
 
+// Per-device caches below are written by whichever host thread first needs
+// the value; every writer computes the same value, and atomics make the
+// concurrent first use by two states on two host threads well defined.
+constexpr int kMaxDevices = 64;
+
 int sm_count(int device)
 {
-    static int cache[64] = {0};
-    if (device < 0 || device >= 64)
+    static std::atomic<int> cache[kMaxDevices];
+    if (device < 0 || device >= kMaxDevices)
         return 1;
-    if (cache[device] == 0) {
-        int c = 0;
+    int c = cache[device].load(std::memory_order_relaxed);
+    if (c == 0) {
         if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || c < 1)
             c = 1;
-        cache[device] = c;
+        cache[device].store(c, std::memory_order_relaxed);
     }
-    return cache[device];
+    return c;
 }
 
 // Resident blocks per SM of a register-path kernel, cached per (kernel, device).
 template <auto Kernel>
 int blocks_per_sm(int device)
 {
-    static int cache[64] = {0};
-    if (device < 0 || device >= 64)
+    static std::atomic<int> cache[kMaxDevices];
+    if (device < 0 || device >= kMaxDevices)
         return 1;
-    if (cache[device] == 0) {
-        int b = 0;
+    int b = cache[device].load(std::memory_order_relaxed);
+    if (b == 0) {
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, Kernel, kThreads, 0) != cudaSuccess || b < 1)
             b = 1;
-        cache[device] = b;
+        cache[device].store(b, std::memory_order_relaxed);
     }
-    return cache[device];
+    return b;
 }
 
 // Persistent grid for a register-path kernel: SMs x resident blocks, fewer
@@ -617,19 +624,34 @@ unsigned grid_for(int device, int64_t n, int cap)
 
 constexpr int kUnrollSq = 2;
 
+// Raise the fused kernel's dynamic shared-memory limit on `device` (once per
+// device; the device must be current).  Setting the attribute also loads the
+// kernel's code on a lazily loading context.
+template <typename G, int R, bool CLIP, bool CHECK>
+cudaError_t prepare_pipeline_kernel(int device)
+{
+    constexpr auto kern = k_grad_reduce_adamw_cast<G, R, CLIP, CHECK>;
+    constexpr uint32_t smem = Pipe<G, R>::kSmemBytes;
+    static std::atomic<int> attr_set[kMaxDevices];
+    if (device >= 0 && device < kMaxDevices && attr_set[device].load(std::memory_order_acquire))
+        return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    if (device >= 0 && device < kMaxDevices)
+        attr_set[device].store(1, std::memory_order_release);
+    return cudaSuccess;
+}
+
 template <typename G, int R, bool CLIP, bool CHECK>
 cudaError_t launch_step_r(const KArgs &a, int device, cudaStream_t stream)
 {
     constexpr auto kern = k_grad_reduce_adamw_cast<G, R, CLIP, CHECK>;
     constexpr uint32_t smem = Pipe<G, R>::kSmemBytes;
     static_assert(smem <= 227 * 1024, "pipeline stages exceed the shared memory of a CTA");
-    static int attr_set[64] = {0};
-    if (device >= 0 && device < 64 && !attr_set[device]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess)
-            return e;
-        attr_set[device] = 1;
-    }
+    cudaError_t e = prepare_pipeline_kernel<G, R, CLIP, CHECK>(device);
+    if (e != cudaSuccess)
+        return e;
     // one CTA per SM, never more CTAs than whole tiles (at least one, for the tail)
     int64_t grid = sm_count(device);
     const int64_t ntiles = a.n / kTile;
@@ -691,12 +713,12 @@ __global__ void k_fill_zero(uint4 *p, size_t n16)
 
 }  // namespace
 
-cudaError_t launch_fill_zero(void *p, size_t bytes, cudaStream_t stream)
+cudaError_t launch_fill_zero(void *p, size_t bytes, int device, cudaStream_t stream)
 {
     const size_t n16 = bytes / 16;
     if (n16 == 0)
         return cudaSuccess;
-    const int dev_blocks = sm_count(0) * 8;
+    const int dev_blocks = sm_count(device) * 8;
     k_fill_zero<<<dev_blocks, kThreads, 0, stream>>>(reinterpret_cast<uint4 *>(p), n16);
     return cudaGetLastError();
 }
@@ -734,6 +756,43 @@ cudaError_t launch_grad_sqnorm(const ReplicaPtrs &g, int R, int64_t n, const Cli
     SqArgs a{g, n, scratch.partials};
     return f32_grads ? launch_sq_g<float>(a, R, n_partials, device, stream)
                      : launch_sq_g<uint16_t>(a, R, n_partials, device, stream);
+}
+
+namespace {
+
+// Load (and prepare) every kernel that a BF16-replica step without the
+// non-finite check can launch: the fused kernel with and without the clip and
+// the clip pre-pass, for R = 1..8.
+template <int R>
+cudaError_t preload_bf16_r(int device)
+{
+    cudaFuncAttributes fa;
+    cudaError_t e = prepare_pipeline_kernel<uint16_t, R, true, false>(device);
+    if (e == cudaSuccess)
+        e = prepare_pipeline_kernel<uint16_t, R, false, false>(device);
+    if (e == cudaSuccess)
+        e = cudaFuncGetAttributes(&fa, k_grad_sqnorm<uint16_t, R, kUnrollSq>);
+    if (e == cudaSuccess)
+        blocks_per_sm<k_grad_sqnorm<uint16_t, R, kUnrollSq>>(device);
+    return e;
+}
+
+}  // namespace
+
+cudaError_t preload_bf16_step_kernels(int device)
+{
+    cudaError_t e = cudaSuccess;
+    if (e == cudaSuccess) e = preload_bf16_r<1>(device);
+    if (e == cudaSuccess) e = preload_bf16_r<2>(device);
+    if (e == cudaSuccess) e = preload_bf16_r<3>(device);
+    if (e == cudaSuccess) e = preload_bf16_r<4>(device);
+    if (e == cudaSuccess) e = preload_bf16_r<5>(device);
+    if (e == cudaSuccess) e = preload_bf16_r<6>(device);
+    if (e == cudaSuccess) e = preload_bf16_r<7>(device);
+    if (e == cudaSuccess) e = preload_bf16_r<8>(device);
+    if (e == cudaSuccess)
+        sm_count(device);
+    return e;
 }
 
 cudaError_t launch_grad_reduce_adamw_cast(const ReplicaPtrs &g, int R, int64_t n, float *theta,

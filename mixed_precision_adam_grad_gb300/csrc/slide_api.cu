@@ -258,7 +258,7 @@ slide_status slide_state_create(const slide_config *cfg, slide_state **out)
         void *dptr = nullptr;
         e = cudaHostGetDevicePointer(&dptr, st->host_arena, 0);
         if (e == cudaSuccess)
-            e = launch_fill_zero(dptr, st->host_bytes, 0);
+            e = launch_fill_zero(dptr, st->host_bytes, st->device, 0);
         if (e == cudaSuccess)
             e = cudaDeviceSynchronize();
         if (e != cudaSuccess) {

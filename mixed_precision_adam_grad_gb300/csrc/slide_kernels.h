@@ -52,7 +52,13 @@ cudaError_t launch_grad_reduce_adamw_cast(const ReplicaPtrs &g, int R, int64_t n
 cudaError_t launch_cast_bf16(const float *src, uint16_t *w, int64_t n, cudaStream_t stream);
 
 // Zero `bytes` (a multiple of 16, 16-byte aligned) of device-accessible memory
-// (device memory, or pinned host memory through its device address).
-cudaError_t launch_fill_zero(void *p, size_t bytes, cudaStream_t stream);
+// (device memory, or pinned host memory through its device address) on
+// `device`, which must be current; the grid is sized from its SM count.
+cudaError_t launch_fill_zero(void *p, size_t bytes, int device, cudaStream_t stream);
+
+// Load every kernel that a BF16-replica step without the non-finite check may
+// launch on `device` (the current device), and fill the per-device launch
+// caches, so that no later step of that kind loads code or queries the device.
+cudaError_t preload_bf16_step_kernels(int device);
 
 }  // namespace slide

@@ -122,3 +122,108 @@ def oracle_sampled(w, unit_index, idx, first_step, last_step, theta, m, v, coefs
         coef = coefs[t] if (w.max_grad_norm > 0) else 1.0
         oracle.adamw_update(gm, coef, theta, m, v, wbf, hp, t)
     return wbf
+
+
+# ---------------------------------------------------- whole-layer runs ----
+# The oracle's functions are single-threaded.  For layers of hundreds of
+# millions of parameters the tests run them on disjoint slices in threads (the
+# ctypes calls release the GIL): every element still goes through exactly the
+# oracle's operations, and the one cross-element quantity, the clip norm, is
+# the oracle's own sum over the whole mean gradient in index order.
+
+import os  # noqa: E402
+from concurrent.futures import ThreadPoolExecutor  # noqa: E402
+
+
+def _workers():
+    return max(1, min(32, os.cpu_count() or 1))
+
+
+def slices(n, parts):
+    """Disjoint [a, b) ranges covering [0, n), 64-element aligned starts."""
+    if n <= 0:
+        return []
+    step = max(1 << 16, -(-n // max(1, parts)))
+    step = (step + 63) // 64 * 64
+    return [(a, min(n, a + step)) for a in range(0, n, step)]
+
+
+def oracle_step_threaded(reps, theta, m, v, w, hp, t):
+    """One oracle layer step over the whole layer, in place (the same result
+    as oracle.layer_step): mean of the replicas, clip coefficient over the
+    whole mean, AdamW update with the BF16 copy.  Returns the coefficient."""
+    n = theta.size
+    nw = _workers()
+    gm = np.empty(n, np.float32)
+    sl = slices(n, 4 * nw)
+
+    def mean(ab):
+        a, b = ab
+        gm[a:b] = oracle.grad_mean([g[a:b] for g in reps])
+
+    def update(ab, coef):
+        a, b = ab
+        oracle.adamw_update(gm[a:b], coef, theta[a:b], m[a:b], v[a:b], None if w is None else w[a:b], hp, t)
+
+    with ThreadPoolExecutor(nw) as ex:
+        list(ex.map(mean, sl))
+        coef = 1.0
+        if hp.max_grad_norm > 0:
+            coef = oracle.clip_coef(oracle.grad_sqnorm(gm), hp.max_grad_norm)
+        list(ex.map(lambda ab: update(ab, coef), sl))
+    return coef
+
+
+def master_threaded(n, seed, unit=0):
+    """The seeded initial master of a whole unit, generated on the host."""
+    out = np.empty(n, np.float32)
+
+    def fill(ab):
+        a, b = ab
+        out[a:b] = synth.master(b - a, seed, unit=unit, offset=a)
+
+    with ThreadPoolExecutor(_workers()) as ex:
+        list(ex.map(fill, slices(n, 4 * _workers())))
+    return out
+
+
+def replicas_to_host(w, unit_index, step, dev_bufs, n, check=4096, seed=0):
+    """Host copies of the R replicas that the seeded generator wrote into the
+    device buffers `dev_bufs` (torch tensors) for (unit, step); a random
+    sample of each is checked against the host generator first, so the
+    oracle's inputs are the generator's values whichever twin produced them."""
+    import torch
+    torch.cuda.synchronize()
+    out = []
+    rng = np.random.default_rng(seed + 7919 * step + unit_index)
+    idx = np.unique(np.concatenate([rng.integers(0, n, size=min(check, n)), [0, n - 1]])).astype(np.int64)
+    for r, buf in enumerate(dev_bufs):
+        h = buf[:n].cpu().numpy()
+        h = h.view(np.float32) if w.fp32_grads else h.view(np.uint16)
+        want = unit_grad_host(w, unit_index, step, r, idx)
+        assert np.array_equal(h[idx].view(np.uint8), want.view(np.uint8)), "device generator disagrees with host"
+        out.append(h)
+    return out
+
+
+def _merge(reports):
+    out = dict(reports[0])
+    for r in reports[1:]:
+        out["n"] += r["n"]
+        out["not_bit_equal"] += r["not_bit_equal"]
+        out["violations"] += r["violations"]
+        for k in ("max_abs", "max_ulp"):
+            if k in out:
+                out[k] = max(out[k], r[k])
+    return out
+
+
+def compare_fp32_all(name, got, want, chunk=1 << 25):
+    """compare_fp32 over every element, in chunks (bounded temporaries)."""
+    n = got.size
+    return _merge([compare_fp32(name, got[a:a + chunk], want[a:a + chunk]) for a in range(0, max(n, 1), chunk)])
+
+
+def compare_bf16_all(name, got, want, chunk=1 << 25):
+    n = got.size
+    return _merge([compare_bf16(name, got[a:a + chunk], want[a:a + chunk]) for a in range(0, max(n, 1), chunk)])

@@ -46,6 +46,27 @@ def test_library_exports_every_declared_symbol(S):
     assert S.slide_abi_version() == 1
 
 
+def test_every_entry_point_cites_its_passage():
+    """Each exported call's comment in include/*.h names the passage that
+    defines it (page title and section), or says that the pages have none."""
+    inc = os.path.join(ROOT, "include")
+    for f in sorted(os.listdir(inc)):
+        if not f.endswith(".h"):
+            continue
+        text = open(os.path.join(inc, f)).read()
+        for m in re.finditer(r"SLIDE_API[^;(]*?\b(slide_\w+)\s*\(", text):
+            # the comment block directly above the declaration
+            before = text[:m.start()].rstrip()
+            assert before.endswith("*/"), f"{m.group(1)} has no comment block"
+            block = re.sub(r"\s*\n\s*\*\s?", " ", before[before.rfind("/*"):])
+            cites = re.search(r"Defined by:|has\s+no counterpart|no\s+passage", block)
+            assert cites, f"{m.group(1)}: its comment cites no passage"
+            if "Defined by:" in block and "no passage" not in block:
+                names = ("SlideDP", "Heterogeneous Co-Design", "Accelerating the", "passage cited above",
+                         "same passages as")
+                assert any(n in block for n in names), f"{m.group(1)}: no page title in its citation"
+
+
 def test_binding_fails_loudly_without_library(S, monkeypatch):
     from mixed_precision_adam_grad_gb300 import _binding
     monkeypatch.setattr(_binding, "LIB_PATH", os.path.join(ROOT, "no_such_libslide.so"))

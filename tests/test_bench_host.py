@@ -101,3 +101,105 @@ def test_streamed_leg_rejects_unknown_layout_suffix():
         streamed_bf16_in_hbm = False
     with pytest.raises(ValueError):
         bench.run_streamed(A(), None, None, None, "h8192x8_streamed+bogus")
+
+
+def _full_record():
+    """A record shaped like run_ours' (values made up, timelines long)."""
+    n, R = 330_311_680, 8
+    units = [{"h2d_begin": 1.0 * i, "master_landed": 1.0 * i + 0.2, "h2d_end": 1.0 * i + 0.9,
+              "update_end": 1.0 * i + 1.0, "d2h_begin": 1.0 * i + 0.3, "d2h_end": 1.0 * i + 1.2} for i in range(42)]
+    streamed = {"workload": "h8192x8_streamed", "description": "x" * 300, "params": 7_021_395_968, "replicas": 8,
+                "steps": 5, "s_per_step": 0.66, "s_per_step_each": [0.66, 0.67, 0.65, 0.7, 0.66],
+                "s_per_step_min": 0.65, "s_per_step_mean": 0.668, "gparam_s": 10.6, "roofline_s": 0.644,
+                "frac": 0.97, "frac_fastest_step": 0.99,
+                "per_step": [{"s": 0.66, "unit_max_over_median": 1.1, "slowest_unit": 3,
+                              "median_unit_copy_in_ms": 80.0}] * 5,
+                "link_bytes_per_step": {"h2d": 14 * 7_021_395_968, "d2h": 14 * 7_021_395_968},
+                "bf16_copy_in_hbm": False, "achieved_link_gbs_each_way": 148.0,
+                "link": {"h2d_gbs": 211.0, "d2h_gbs": 193.0, "h2d_concurrent_gbs": 171.0,
+                         "d2h_concurrent_gbs": 170.0, "bidir_gbs": 340.0, "probe": "p"},
+                "link_monitor_before": {"h2d": {"median_gbs": 168.0}}, "link_monitor_after": {},
+                "host_pinned_gb": 98.3, "window_gb": 52.7, "create_s": 10.0, "chunk_mib": 64,
+                "grad_callback": "g" * 200, "s_per_step_with_generator_callback": 1.23,
+                "cpu_baseline": {"value": 0.05, "unit": "Gparam/s", "cores": 1, "kind": "oracle",
+                                 "s_per_step_extrapolated": 140.0, "sample": "s" * 300},
+                "timeline_fastest_step": {"units_ms": units}, "timeline_slowest_step": {"units_ms": units},
+                "bf16_delivery": {"full": {"ms": 66.4}}, "timing": "t"}
+    hbm = {"workload": "h2560_R4_clip", "description": "d", "params": 100_930_560, "replicas": 4, "steps": 20,
+           "value": 155.0, "unit": "Gparam/s", "ms_per_step": 0.65, "hbm_gbs": 6500.0,
+           "roofline": {"bound": "hbm", "kernel": "grad_reduce_adamw_cast", "achieved": 6700.0, "peak": 6779.0,
+                        "unit": "GB/s", "frac": 0.988, "traffic": None, "traffic_note": "n",
+                        "bytes_per_launch": 34 * 100_930_560, "bytes_per_param": 34, "avg_launch_ms": 0.51,
+                        "launches": 20},
+           "prepass": {"achieved": 5900.0, "frac": 0.87, "avg_launch_ms": 0.137, "bytes_per_param": 8},
+           "step_roofline_frac": 0.96}
+    bytes_upd = 42 * n
+    avg = 2.07
+    ach = bytes_upd / (avg * 1e-3) / 1e9
+    return {
+        "metric": bench.METRIC, "value": 159.3, "unit": "Gparam/s", "n_gpus": 1, "steps": 20, "warmup": 5,
+        "ms_per_step": 2.074, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "h5120_R8_logscale", "description": "one h=5120 decoder layer", "params": n,
+                   "replicas": R, "max_grad_norm": 0.0, "parallelism": "replicas-only x1", "l2": "larger",
+                   "clock_samples": "c"},
+        "hbm_gbs": 6690.0,
+        "roofline": {"bound": "hbm", "kernel": "grad_reduce_adamw_cast", "achieved": ach, "peak": 6779.0,
+                     "unit": "GB/s", "frac": ach / 6779.0, "traffic": 13.6e9, "traffic_note": "ncu",
+                     "peak_kind": "measured (MEASURED_PEAKS.json hbm_gbs)", "bytes_per_launch": bytes_upd,
+                     "avg_launch_ms": avg, "bytes_per_param": 42, "launches": 20},
+        "prepass": None, "step_roofline_frac": 0.98, "gpu_launches": 20,
+        "clocks": {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 9},
+        "e2e": {"value": 12.0, "unit": "Gparam/s", "h2d_bytes_per_step": 2 * R * n, "d2h_bytes_per_step": 2 * n,
+                "steps": 20, "pipelining": "p" * 100},
+        "cpu_baseline": {"value": 0.05, "unit": "Gparam/s", "cores": 1, "kind": "oracle", "gbs": 2.1,
+                         "gbs_bytes_per_param": 42, "cpu_model": "Neoverse-V2", "sample": "s" * 400},
+        "cpu_baseline_all_cores": {"value": 0.8, "unit": "Gparam/s", "cores": 16, "kind": "oracle_openmp",
+                                   "gbs": 33.0, "gbs_bytes_per_param": 42, "cpu_model": "Neoverse-V2",
+                                   "sample": "s"},
+        "fp32_grad_variant": dict(hbm, workload="h2560_R4_clip_fp32grads"),
+        "other_hbm_workloads": {"h2560_R1": dict(hbm, workload="h2560_R1", prepass=None),
+                                "h2560_R4_clip": hbm},
+        "cpu_reduce_route": {"params": n, "replicas": R, "identical_results": True,
+                             "gpu_route": {"s": 0.002, "link_bytes": 0},
+                             "cpu_route": {"s": 3.0, "d2h_bytes": 2 * R * n, "h2d_bytes": 4 * n,
+                                           "link_bytes": 2 * R * n + 4 * n}},
+        "chunk_sweep": {"workload": "h8192x8_streamed", "chosen": [64, 64],
+                        "points": [{"h2d_mib": a, "d2h_mib": b, "frac": 0.9, "s_per_step": 0.7}
+                                   for a in (16, 32, 64, 128) for b in (16, 64, 256)]},
+        "streamed": streamed,
+        "streamed_also": {"h5120x40_streamed": dict(streamed, workload="h5120x40_streamed",
+                                                    bf16_copy_in_hbm=True),
+                          "h8192x8_streamed+bf16hbm": dict(streamed, bf16_copy_in_hbm=True),
+                          "h8192x8_streamed+x": {"workload": "h8192x8_streamed", "skipped": "host memory " * 40}},
+    }
+
+
+def test_compact_headline_is_last_and_small(capsys, tmp_path):
+    import json
+    full = _full_record()
+    out = tmp_path / "detail.json"
+    bench.report(full, str(out))
+    lines = capsys.readouterr().out.strip().splitlines()
+    last = lines[-1]
+    assert len(last.encode()) < 4096, len(last.encode())
+    assert all(x.startswith("detail ") for x in lines[:-1])
+    h = json.loads(last)
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "cpu_baseline", "e2e", "clocks",
+              "gpu_launches"):
+        assert k in h, k
+    assert h["config"]["workload"] == "h5120_R8_logscale"
+    rf = h["roofline"]
+    # frac recomputes from the line's own fields (to the rounding of 4 digits)
+    ach = rf["bytes_per_launch"] / (rf["avg_launch_ms"] * 1e-3) / 1e9
+    assert abs(ach / rf["achieved"] - 1) < 1e-3
+    assert abs(rf["achieved"] / rf["peak"] / rf["frac"] - 1) < 1e-3
+    assert rf["launches"] == 20
+    assert h["e2e"]["h2d_bytes_per_step"] == 16 * 330_311_680
+    st = h["streamed"]
+    assert st["h8192x8_streamed"]["frac"] == 0.97 and st["h8192x8_streamed"]["unit_max_over_median"] == 1.1
+    assert "skipped" in st["h8192x8_streamed+x"]
+    assert st["h5120x40_streamed"]["bf16_in_hbm"] is True
+    assert len(h["chunk_sweep"]["points"]) == 12
+    assert json.load(open(out))["streamed"]["timeline_fastest_step"]["units_ms"][0]["h2d_begin"] == 0.0

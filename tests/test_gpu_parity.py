@@ -2,9 +2,9 @@
 element on identical seeded inputs.
 
 Small sizes compare every element (they span several blocks' tiles and a
-ragged tail); the full-size workloads compare sampled elements, which the
-oracle computes one by one (the update is elementwise once the clip
-coefficient, which the oracle forms over the whole layer, is known).
+ragged tail); so do the full-size HBM workloads, whose oracle runs over the
+whole unit (its functions on disjoint slices in threads, the clip norm over
+the whole mean gradient).
 
 Gate: |gpu - oracle| <= 2e-6*(1+|oracle|) on FP32 master, m, v after every
 step, and <= 1 BF16 ulp on the emitted copy.  Without the clip the two
@@ -286,68 +286,62 @@ def test_state_allocation_matches_accounting(S):
         S.slide_state_destroy(st)
 
 
-# -------------------------------------------- full-size workloads, sampled ----
+# ---------------------------------------- full-size workloads, every element ----
 
-def run_full_size(S, w, n_samples=200_000):
+def run_full_size(S, w):
     """The workload's single HBM-resident unit at full size, in the launch
-    configuration the benchmark times (the library picks it); the oracle on
-    sampled elements, with whole-unit clip coefficients when the clip is on."""
+    configuration the benchmark times (the library picks it), against the
+    oracle run over the whole unit on the same seeded inputs: every element
+    of master, m, v and the BF16 copy after the last step, and the clip
+    coefficient of every step."""
     assert len(w.units) == 1
     n = w.units[0].numel
-    bounds = np.cumsum([0] + [k for _, k in w.units[0].tensors])
-    idx = pu.sample_indices(n, n_samples, extra=np.concatenate([bounds - 1, bounds]))
-    t0 = 0
-    th_s = synth.gather_master(idx, w.seed)
-    m_s, v_s = np.zeros(idx.size, np.float32), np.zeros(idx.size, np.float32)
+    hp_or = pu.hp_oracle(w)
+    th = pu.master_threaded(n, w.seed)
+    m, v, wb = np.zeros(n, np.float32), np.zeros(n, np.float32), np.zeros(n, np.uint16)
+    grads = [dev_grad_buf(n, w.fp32_grads) for _ in range(w.R)]
     st = S.slide_state_create([n], w.R, flags=S.SLIDE_FLAG_FP32_GRADS if w.fp32_grads else 0)
     try:
-        th_d = S.slide_layer_ptrs(st, 0)[0]
-        synth.dev_master(th_d, n, w.seed)
-        torch.cuda.synchronize()
-        coefs = None
-        if w.max_grad_norm > 0:
-            coefs = pu.oracle_full_coefs(w, 0, range(1, w.prewarm_steps + w.steps + 1))
+        t0 = 0
         if w.prewarm_steps:
-            # pre-warm by the oracle over the whole unit, handed to the state
-            hp_or = pu.hp_oracle(w)
-            th = synth.master(n, w.seed)
-            m, v = np.zeros(n, np.float32), np.zeros(n, np.float32)
+            # pre-warm m and v by the oracle over the whole unit, handed to the state
             for t in range(1, w.prewarm_steps + 1):
-                reps = [pu.unit_grad_host(w, 0, t, r) for r in range(w.R)]
-                gm = oracle.grad_mean(reps)
+                for r in range(w.R):
+                    pu.unit_grad_dev(w, 0, t, r, grads[r].data_ptr())
+                reps = pu.replicas_to_host(w, 0, t, grads, n)
+                pu.oracle_step_threaded(reps, th, m, v, None, hp_or, t)
                 del reps
-                oracle.adamw_update(gm, coefs[t], th, m, v, None, hp_or, t)
-                del gm
             S.slide_layer_set(st, 0, th, m, v, step=w.prewarm_steps)
-            th_s, m_s, v_s = th[idx].copy(), m[idx].copy(), v[idx].copy()
-            del th, m, v
             t0 = w.prewarm_steps
-        grads = [dev_grad_buf(n, w.fp32_grads) for _ in range(w.R)]
+        else:
+            synth.dev_master(S.slide_layer_ptrs(st, 0)[0], n, w.seed)   # the device twin of the same master
         hp = S.hparams(*w.hparams_tuple())
         for t in range(t0 + 1, t0 + w.steps + 1):
             for r in range(w.R):
                 pu.unit_grad_dev(w, 0, t, r, grads[r].data_ptr())
             S.slide_layer_step(st, 0, grads, hp)
-            if coefs is not None:
+            reps = pu.replicas_to_host(w, 0, t, grads, n)
+            coef = pu.oracle_step_threaded(reps, th, m, v, wb, hp_or, t)
+            del reps
+            if w.max_grad_norm > 0:
                 gc = S.slide_layer_last_clip_coef(st, 0)
-                assert abs(gc - coefs[t]) <= 2 * np.spacing(np.float32(coefs[t])), (t, gc, coefs[t])
-        w_s = pu.oracle_sampled(w, 0, idx, t0 + 1, t0 + w.steps, th_s, m_s, v_s, coefs)
-        th_a, m_a, v_a = (np.empty(n, np.float32) for _ in range(3))
-        w_a = np.empty(n, np.uint16)
-        assert S.slide_layer_get(st, 0, th_a, m_a, v_a, w_a) == t0 + w.steps
-        th_g, m_g, v_g, w_g = th_a[idx], m_a[idx], v_a[idx], w_a[idx]
-        del th_a, m_a, v_a, w_a
-        rep = [pu.compare_fp32("theta", th_g, th_s), pu.compare_fp32("m", m_g, m_s),
-               pu.compare_fp32("v", v_g, v_s), pu.compare_bf16("w", w_g, w_s)]
+                assert abs(gc - coef) <= 2 * np.spacing(np.float32(coef)), (t, gc, coef)
+        th_g, m_g, v_g = (np.empty(n, np.float32) for _ in range(3))
+        w_g = np.empty(n, np.uint16)
+        assert S.slide_layer_get(st, 0, th_g, m_g, v_g, w_g) == t0 + w.steps
+        rep = [pu.compare_fp32_all("theta", th_g, th), pu.compare_fp32_all("m", m_g, m),
+               pu.compare_fp32_all("v", v_g, v), pu.compare_bf16_all("w", w_g, wb)]
         pu.assert_parity(rep)
         assert np.array_equal(w_g, oracle.f32_to_bf16(th_g))
+        if w.max_grad_norm <= 0:   # same FP32 operations on both sides without the clip
+            assert all(r["not_bit_equal"] == 0 for r in rep), rep
         return rep
     finally:
         S.slide_state_destroy(st)
 
 
 @pytest.mark.parametrize("name", ["h2560_R1", "h2560_R4_clip", "h5120_R8_logscale", "h2560_R4_clip_fp32grads"])
-def test_full_size_workload_sampled(S, name):
+def test_full_size_workload_every_element(S, name):
     w = W.ALL[name]()
     rep = run_full_size(S, w)
     print(rep)
