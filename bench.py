@@ -68,8 +68,20 @@ def parse_args():
     ap.add_argument("--streamed-steps", type=int, default=5)
     ap.add_argument("--streamed-bf16-in-hbm", action="store_true",
                     help="keep the BF16 copy in HBM (host holds 12 B/param); implied for h5120x40_streamed")
+    ap.add_argument("--pinned-guard-gib", type=int, default=8,
+                    help="pin this many GiB first and hold them for the run (0: none); see PinnedArena")
+    ap.add_argument("--streamed-arena", choices=["hostalloc", "hugepages"], default="hostalloc",
+                    help="pinned host arena of the streamed legs: cudaHostAlloc, or an anonymous mapping "
+                         "advised for transparent huge pages and registered with cudaHostRegister")
     ap.add_argument("--streamed-chunk-mib", type=int, default=64,
-                    help="copy chunk of the streamed engine (the pages' 64 MiB by default)")
+                    help="host->device copy chunk of the streamed engine (the pages' 64 MiB by default)")
+    ap.add_argument("--streamed-chunk-d2h-mib", type=int, default=0,
+                    help="device->host write-back chunk of the streamed engine (0: as the copy-in chunk)")
+    ap.add_argument("--chunk-sweep", default="32:32,64:64,128:128,256:256,512:512,64:256,256:64,128:512",
+                    help="copy-in:write-back chunk sizes (MiB) swept on each --chunk-sweep-workloads "
+                         "workload ('' for none)")
+    ap.add_argument("--chunk-sweep-workloads", default="h8192x8_streamed,h5120x40_streamed",
+                    help="streamed workloads of the chunk sweep (each must fit the run's pinned arena)")
     ap.add_argument("--batches", type=int, default=4,
                     help="pre-generated gradient batches cycled by the steps (1 for small profiling runs)")
     ap.add_argument("--slice-params", type=int, default=0,
@@ -354,11 +366,51 @@ def mem_available_bytes():
     return 0
 
 
-def link_probe(torch, nbytes=1 << 30, reps=20):
+def release_pinned_cache(torch):
+    """Return the pinned host buffers that torch keeps cached after their
+    tensors are freed, so the streamed legs can pin the host state."""
+    import gc
+    gc.collect()
+    fn = getattr(torch._C, "_host_emptyCache", None)
+    if fn is not None:
+        fn()
+
+
+def anon_huge_kb(addr):
+    """AnonHugePages (kB) of the mapping of this process that holds addr
+    (from /proc/self/smaps), or None where that cannot be read."""
+    try:
+        with open("/proc/self/smaps") as f:
+            inside = False
+            for line in f:
+                head = line.split()
+                if head and "-" in head[0] and len(head) >= 5 and not head[0].endswith(":"):
+                    lo, hi = (int(x, 16) for x in head[0].split("-"))
+                    inside = lo <= addr < hi
+                elif inside and line.startswith("AnonHugePages:"):
+                    return int(line.split()[1])
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+def pinned_empty(torch, arena=None):
+    """Allocator of pinned host tensors: carved from the run's arena when
+    there is one, else torch's pinned allocator."""
+    if arena is not None:
+        return lambda shape, dtype: arena.tensor(shape, dtype)
+    return lambda shape, dtype: torch.empty(shape, dtype=dtype, pin_memory=True)
+
+
+PROBE_BYTES = (2 << 30) + (1 << 30) + (1 << 20)   # link probe and link monitor buffers
+
+
+def link_probe(torch, nbytes=1 << 30, reps=20, arena=None):
     """Pinned host <-> device copy bandwidth (GB/s): each direction alone,
     then both at once on two streams (per direction and aggregate); medians."""
-    h_src = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
-    h_dst = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    alloc = pinned_empty(torch, arena)
+    h_src = alloc(nbytes, torch.uint8)
+    h_dst = alloc(nbytes, torch.uint8)
     d_dst = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     d_src = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
@@ -405,15 +457,16 @@ def link_probe(torch, nbytes=1 << 30, reps=20):
     return out
 
 
-def link_monitor(torch, seconds=2.0, chunk=64 << 20, slots=8):
+def link_monitor(torch, seconds=2.0, chunk=64 << 20, slots=8, arena=None):
     """Both directions of the host link kept busy for `seconds` with
     back-to-back pinned <-> device copies of `chunk` bytes, every copy timed
     by its own pair of events.  The per-copy rates over time show whether the
     link held its rate for the whole window: on a host shared with other
     work it can drop for stretches of a few hundred ms, which a median-based
     probe hides.  Rates in GB/s; a copy is "slow" below 0.8 x the median."""
-    h_src = torch.empty(slots, chunk, dtype=torch.uint8, pin_memory=True)
-    h_dst = torch.empty(slots, chunk, dtype=torch.uint8, pin_memory=True)
+    alloc = pinned_empty(torch, arena)
+    h_src = alloc((slots, chunk), torch.uint8)
+    h_dst = alloc((slots, chunk), torch.uint8)
     d_dst = torch.empty(slots, chunk, dtype=torch.uint8, device="cuda")
     d_src = torch.empty(slots, chunk, dtype=torch.uint8, device="cuda")
     s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
@@ -451,19 +504,21 @@ def link_monitor(torch, seconds=2.0, chunk=64 << 20, slots=8):
     return out
 
 
-def unit_spread(units):
-    """Longest unit copy-in of a streamed step against the median unit (the
-    first and last units of the sweep excluded: they have no neighbour on one
-    side): a ratio near 1 means every unit met the same link rate."""
+def unit_spread(units, sizes=None):
+    """Slowest unit copy-in of a streamed step against the median unit, per
+    parameter (sizes: parameters per unit; equal sizes if None): a ratio near
+    1 means every unit met the same link rate.  Every unit of the sweep
+    counts, the first and the last included."""
     import math
-    inner = [(i, u["h2d_end"] - u["h2d_begin"]) for i, u in enumerate(units[1:-1], 1)
-             if not math.isnan(u["h2d_begin"])]
-    if not inner:
+    sizes = sizes or [1] * len(units)
+    rates = [(i, (u["h2d_end"] - u["h2d_begin"]) / max(1, sizes[i])) for i, u in enumerate(units)
+             if not math.isnan(u["h2d_begin"]) and sizes[i] > 0]
+    if len(rates) < 2:
         return {"unit_max_over_median": None, "slowest_unit": None}
-    med = statistics.median(t for _, t in inner)
-    i, t = max(inner, key=lambda x: x[1])
+    med = statistics.median(t for _, t in rates)
+    i, t = max(rates, key=lambda x: x[1])
     return {"unit_max_over_median": t / med if med > 0 else None, "slowest_unit": i,
-            "median_unit_copy_in_ms": med}
+            "median_unit_copy_in_ms_per_gparam": med * 1e9}
 
 
 def _union(intervals):
@@ -518,13 +573,168 @@ def measure_delivery(S, torch, st, layer, n, R, reps=3):
     return out
 
 
-def run_streamed(args, S, torch, synth, key):
+class PinnedArena:
+    """The run's one pinned host allocation, of an exact size (cudaHostAlloc,
+    portable and mapped), made before anything else is pinned.  The legs take
+    their DMA-only host buffers from it in turn: the end-to-end leg's replicas
+    and copy, the link probes' buffers and each streamed state's host state
+    (handed to the library as its host_arena).  So the streamed states get
+    pages that no earlier buffer used and that the CPU never touched: on these
+    hosts, pinned pages that the CPU had read or written, including pages that
+    earlier pinned buffers had left behind, were read several times slower by
+    the copy engines for a while afterwards.
+
+    The same class pins the run's guard block first of all: on these hosts
+    (virtual machines) a fixed set of about 7 GiB of guest memory, which a
+    fresh machine hands to the first pinned allocation, decays within a minute
+    of being pinned to about 15 GB/s of copy-engine reads while the rest holds
+    210 GB/s.  The guard holds those pages for the run and is not used."""
+
+    def __init__(self, nbytes):
+        import ctypes as C
+        import ctypes.util
+        lib = None
+        for name in ("libcudart.so.13", ctypes.util.find_library("cudart") or "", "libcudart.so"):
+            if not name:
+                continue
+            try:
+                lib = C.CDLL(name)
+                break
+            except OSError:
+                continue
+        if lib is None:
+            raise OSError("libcudart not found")
+        self._lib = lib
+        lib.cudaHostAlloc.argtypes = [C.POINTER(C.c_void_p), C.c_size_t, C.c_uint]
+        lib.cudaFreeHost.argtypes = [C.c_void_p]
+        p = C.c_void_p()
+        t0 = time.time()
+        rc = lib.cudaHostAlloc(C.byref(p), C.c_size_t(nbytes), 1 | 2)   # portable | mapped
+        if rc != 0 or not p.value:
+            raise MemoryError(f"cudaHostAlloc({nbytes}) failed with {rc}")
+        self.addr, self.nbytes, self.pin_s = p.value, nbytes, time.time() - t0
+        self.top = 0
+
+    def mark(self):
+        return self.top
+
+    def reset(self, mark=0):
+        self.top = mark
+
+    def carve(self, nbytes):
+        """Address of the next nbytes (256-byte aligned) of the arena."""
+        a = (self.top + 255) // 256 * 256
+        if a + nbytes > self.nbytes:
+            raise MemoryError(f"pinned arena: {nbytes} bytes do not fit ({self.nbytes - a} left)")
+        self.top = a + nbytes
+        return self.addr + a
+
+    def tensor(self, shape, dtype):
+        """A CPU tensor over the next bytes of the arena (pinned memory)."""
+        import ctypes as C
+        import torch
+        shape = tuple(shape) if isinstance(shape, (tuple, list)) else (shape,)
+        numel = 1
+        for d in shape:
+            numel *= d
+        nbytes = numel * torch.empty((), dtype=dtype).element_size()
+        addr = self.carve(max(nbytes, 1))
+        buf = (C.c_uint8 * max(nbytes, 1)).from_address(addr)
+        return torch.frombuffer(buf, dtype=torch.uint8)[:nbytes].view(dtype).view(shape)
+
+    def free(self):
+        if self.addr:
+            self._lib.cudaFreeHost(self.addr)
+            self.addr = 0
+
+
+def streamed_host_bytes(S, key, args):
+    """Pinned host bytes of a streamed leg (its workload and layout)."""
+    name, _, layout = key.partition("+")
+    w = workload(name)
+    in_hbm = args.streamed_bf16_in_hbm or name == "h5120x40_streamed" or layout == "bf16hbm"
+    flags = S.SLIDE_FLAG_BF16_COPY_IN_HBM if in_hbm else 0
+    return S.slide_state_bytes([u.numel for u in w.units], w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED,
+                               flags=flags)[1]
+
+
+def grad_pool(torch, synth, w, maxn, n_pool=2):
+    """Pre-generated replicas in HBM (the workload's distribution) and the
+    callback argument that copies them into the window for every unit."""
+    import ctypes as C
+    sp = synth.spec(w.seed, w.grad_kind, w.zero_prob)
+    pool = [torch.empty(maxn + 64, dtype=torch.int16, device="cuda") for _ in range(n_pool * w.R)]
+    for k in range(n_pool):
+        for r in range(w.R):
+            synth.dev_grad(pool[k * w.R + r].data_ptr(), maxn, sp, 1000 + k, 0, r, w.grad_scale)
+    torch.cuda.synchronize()
+    sizes = [u.numel for u in w.units]
+    numel = (C.c_int64 * len(sizes))(*sizes)
+    pool_ptrs = (C.c_void_p * len(pool))(*[t.data_ptr() for t in pool])
+    pg = synth.PoolGrads(w.R, n_pool, 0, 0, C.cast(numel, C.c_void_p), C.cast(pool_ptrs, C.c_void_p))
+    return pg, (pool, numel, pool_ptrs)
+
+
+def link_roofline_s(link, N, in_hbm):
+    """T_roof of one streamed step of N parameters for the measured link."""
+    G = 1e9
+    if in_hbm:   # the BF16 copy's delivery and write-back stay inside HBM
+        return max(12 * N / (link["h2d_concurrent_gbs"] * G), 12 * N / (link["d2h_concurrent_gbs"] * G),
+                   24 * N / (link["bidir_gbs"] * G))
+    return (2 * N / (link["h2d_gbs"] * G)
+            + max(12 * N / (link["h2d_concurrent_gbs"] * G), 14 * N / (link["d2h_concurrent_gbs"] * G),
+                  26 * N / (link["bidir_gbs"] * G)))
+
+
+def run_chunk_sweep(args, S, torch, synth, key, arena, link, points, steps=2):
+    """TuneChunks-style sweep of the streamed engine's copy-in (host->device)
+    and write-back (device->host) chunk sizes on one streamed workload: per
+    point, a state on the run's pinned arena, one warm-up step and `steps`
+    timed steps; s/step (median) against the link roofline of the run."""
+    name, _, layout = key.partition("+")
+    w = workload(name)
+    sizes = [u.numel for u in w.units]
+    N = sum(sizes)
+    in_hbm = name == "h5120x40_streamed" or layout == "bf16hbm"
+    flags = S.SLIDE_FLAG_BF16_COPY_IN_HBM if in_hbm else 0
+    pg, keep = grad_pool(torch, synth, w, max(sizes))
+    hp = S.hparams(*w.hparams_tuple())
+    t_roof = link_roofline_s(link, N, in_hbm)
+    out = []
+    for h2d_mib, d2h_mib in points:
+        host_b = S.slide_state_bytes(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED, flags=flags)[1]
+        st = S.slide_state_create(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED,
+                                  chunk_bytes=h2d_mib << 20, chunk_bytes_d2h=d2h_mib << 20, flags=flags,
+                                  host_arena=arena.addr, host_arena_bytes=host_b)
+        try:
+            S.slide_model_step_streamed(st, synth.pool_grad_fn_address(), pg, hp)     # warm-up
+            times, spreads = [], []
+            for k in range(steps):
+                pg.step = 1 + k
+                t0 = time.perf_counter()
+                S.slide_model_step_streamed(st, synth.pool_grad_fn_address(), pg, hp)
+                times.append(time.perf_counter() - t0)
+                spreads.append(unit_spread(S.slide_streamed_timeline(st)[0], sizes)["unit_max_over_median"])
+        finally:
+            S.slide_state_destroy(st)
+        med = statistics.median(times)
+        out.append({"h2d_mib": h2d_mib, "d2h_mib": d2h_mib, "s_per_step": med, "frac": t_roof / med,
+                    "unit_max_over_median": max(x for x in spreads if x is not None) if any(spreads) else None})
+    del keep
+    best = max(out, key=lambda p: p["frac"])
+    return {"workload": key, "roofline_s": t_roof, "steps_per_point": steps, "points": out,
+            "chosen": [best["h2d_mib"], best["d2h_mib"]],
+            "note": "every point runs on the run's one pinned arena; master, m and v start at zero"}
+
+
+def run_streamed(args, S, torch, synth, key, arena=None):
     """Host-resident streamed step of a whole model: s/step against the
     host-link roofline measured in the same run.  The gradient callback stands
     in for the backward pass; in the timed steps it copies pre-generated
     replicas (the workload's distribution) from a pool in HBM into the window,
     so the time is the engine's copies and update; one more step with the
-    on-the-fly generator as the callback is reported beside it."""
+    on-the-fly generator as the callback is reported beside it.  `arena`: a
+    PinnedArena to hold the host state (else the state pins its own)."""
     import ctypes as C
     name, _, layout = key.partition("+")
     if layout not in ("", "bf16hbm"):
@@ -535,29 +745,45 @@ def run_streamed(args, S, torch, synth, key):
     maxn = max(sizes)
     in_hbm = args.streamed_bf16_in_hbm or name == "h5120x40_streamed" or layout == "bf16hbm"
     flags = S.SLIDE_FLAG_BF16_COPY_IN_HBM if in_hbm else 0
+    arena_kind = "the run's one pinned arena (state handed over as host_arena)" if arena else \
+        getattr(args, "streamed_arena", "hostalloc")
+    if arena_kind == "hugepages":
+        flags |= S.SLIDE_FLAG_HOST_HUGE_PAGES
     _, host_b = S.slide_state_bytes(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED, flags=flags)
-    need = host_b + (24 << 30)
+    if arena is not None and arena.nbytes < host_b:
+        return {"workload": w.name, "skipped": f"the run's pinned arena ({arena.nbytes / 1e9:.1f} GB) is smaller "
+                                                f"than this leg's {host_b / 1e9:.1f} GB"}
+    # with the run's arena the host state is pinned already: only working room is needed
+    headroom = (6 << 30) if arena is not None else (24 << 30)
+    need = (0 if arena is not None else host_b) + headroom
     if mem_available_bytes() < need:
-        return {"workload": w.name, "skipped": f"host memory: {host_b / 1e9:.1f} GB pinned + 24 GiB headroom "
-                                                f"needed, {mem_available_bytes() / 1e9:.1f} GB available"}
-    link = link_probe(torch)
-    monitor_before = link_monitor(torch)
+        return {"workload": w.name, "skipped": f"host memory: {(need - headroom) / 1e9:.1f} GB to pin + "
+                                                f"{headroom >> 30} GiB headroom needed, "
+                                                f"{mem_available_bytes() / 1e9:.1f} GB available"}
+    leg_mark = arena.mark() if arena is not None else 0
+    state_addr = arena.carve(host_b) if arena is not None else None
+    probe_mark = arena.mark() if arena is not None else 0
+    link = link_probe(torch, arena=arena)
+    if arena is not None:
+        arena.reset(probe_mark)
+    monitor_before = link_monitor(torch, arena=arena)
+    if arena is not None:
+        arena.reset(probe_mark)
+    release_pinned_cache(torch)
     n_pool = 2
     sp = synth.spec(w.seed, w.grad_kind, w.zero_prob)
-    pool = [torch.empty(maxn + 64, dtype=torch.int16, device="cuda") for _ in range(n_pool * w.R)]
-    for k in range(n_pool):
-        for r in range(w.R):
-            synth.dev_grad(pool[k * w.R + r].data_ptr(), maxn, sp, 1000 + k, 0, r, w.grad_scale)
-    torch.cuda.synchronize()
+    pg, pool_keep = grad_pool(torch, synth, w, maxn, n_pool)
     numel = (C.c_int64 * len(sizes))(*sizes)
-    pool_ptrs = (C.c_void_p * len(pool))(*[t.data_ptr() for t in pool])
-    pg = synth.PoolGrads(w.R, n_pool, 0, 0, C.cast(numel, C.c_void_p), C.cast(pool_ptrs, C.c_void_p))
     mg = synth.ModelGrads(sp, len(sizes), w.R, 1, 0, C.cast(numel, C.c_void_p), None, None, None, None,
                           w.grad_scale)
+    chunk_h2d = args.streamed_chunk_mib
+    chunk_d2h = getattr(args, "streamed_chunk_d2h_mib", 0) or chunk_h2d
     t0 = time.time()
     st = S.slide_state_create(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED,
-                              chunk_bytes=args.streamed_chunk_mib << 20, flags=flags)
+                              chunk_bytes=chunk_h2d << 20, chunk_bytes_d2h=chunk_d2h << 20, flags=flags,
+                              host_arena=state_addr, host_arena_bytes=host_b if arena else 0)
     create_s = time.time() - t0
+    arena_hp_kb = anon_huge_kb(S.slide_layer_ptrs(st, 0)[0])
     try:
         for ui, u in enumerate(w.units):
             synth.dev_master(S.slide_layer_ptrs(st, ui)[0], u.numel, w.seed, unit=ui)
@@ -573,8 +799,10 @@ def run_streamed(args, S, torch, synth, key):
             times.append(time.perf_counter() - t0)
             units_tl, fwd_end = S.slide_streamed_timeline(st)
             tls.append((units_tl, fwd_end))
-            per_step.append(dict(s=times[-1], **unit_spread(units_tl)))
-        monitor_after = link_monitor(torch)
+            per_step.append(dict(s=times[-1], **unit_spread(units_tl, sizes)))
+        monitor_after = link_monitor(torch, arena=arena)
+        if arena is not None:
+            arena.reset(probe_mark)
         fastest, slowest = times.index(min(times)), times.index(max(times))
         overlap_fast = timeline_overlap(*tls[fastest])
         overlap_slow = timeline_overlap(*tls[slowest])
@@ -585,7 +813,9 @@ def run_streamed(args, S, torch, synth, key):
         dev_b = S.slide_state_bytes(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED, flags=flags)[0]
     finally:
         S.slide_state_destroy(st)
-        del pool
+        del pool_keep
+        if arena is not None:
+            arena.reset(leg_mark)
     s_step = statistics.median(times)
     cpu = None
     if not args.no_cpu_baseline:
@@ -596,16 +826,8 @@ def run_streamed(args, S, torch, synth, key):
                "sample": f"first {n_s} parameters of one unit as a layer of their own, R={w.R}, "
                          f"{c_steps} steps ({c_el:.1f} s of single-thread CPU time); the per-parameter rate "
                          f"is extrapolated to the whole model's {N} parameters"}
-    G = 1e9
-    if in_hbm:   # the BF16 copy's delivery and write-back stay inside HBM
-        t_roof = max(12 * N / (link["h2d_concurrent_gbs"] * G), 12 * N / (link["d2h_concurrent_gbs"] * G),
-                     24 * N / (link["bidir_gbs"] * G))
-        per_dir = 12 * N
-    else:
-        t_roof = (2 * N / (link["h2d_gbs"] * G)
-                  + max(12 * N / (link["h2d_concurrent_gbs"] * G), 14 * N / (link["d2h_concurrent_gbs"] * G),
-                        26 * N / (link["bidir_gbs"] * G)))
-        per_dir = 14 * N
+    t_roof = link_roofline_s(link, N, in_hbm)
+    per_dir = 12 * N if in_hbm else 14 * N
     return {"workload": w.name, "description": w.description, "params": N, "replicas": w.R,
             "steps": args.streamed_steps, "s_per_step": s_step, "s_per_step_each": times,
             "s_per_step_min": min(times), "s_per_step_mean": statistics.mean(times),
@@ -615,7 +837,9 @@ def run_streamed(args, S, torch, synth, key):
             "achieved_link_gbs_each_way": per_dir / s_step / 1e9,
             "link": link, "link_monitor_before": monitor_before, "link_monitor_after": monitor_after,
             "host_pinned_gb": host_b / 1e9, "window_gb": dev_b / 1e9,
-            "create_s": create_s, "chunk_mib": args.streamed_chunk_mib,
+            "create_s": create_s, "chunk_mib": chunk_h2d, "chunk_h2d_mib": chunk_h2d, "chunk_d2h_mib": chunk_d2h,
+            "pinned_arena": arena_kind, "arena_pin_s": arena.pin_s if arena else None,
+            "arena_huge_page_kb": arena_hp_kb,
             "grad_callback": f"copies pre-generated replicas ({n_pool} sets, the workload's distribution) "
                              "from HBM into the window",
             "s_per_step_with_generator_callback": gen_s,
@@ -648,6 +872,23 @@ def run_ours(args):
     clip = w.max_grad_norm > 0
     hp = S.hparams(*w.hparams_tuple())
     stream = torch.cuda.Stream()
+
+    # The run's one pinned host arena, pinned before anything else: large
+    # enough for the end-to-end leg and the largest streamed leg that fits the
+    # host (legs use it one after another; only DMA touches it).
+    arena = guard = None
+    streamed_keys = []
+    if world == 1:
+        also = [x for x in args.streamed_also.split(",") if x and x != args.streamed_workload]
+        streamed_keys = [] if args.no_streamed else [args.streamed_workload] + also
+        needs = [0 if args.no_e2e else 2 * (2 * R * n + 2 * n) + (1 << 20)]
+        if args.pinned_guard_gib > 0 and (streamed_keys or not args.no_e2e):
+            guard = PinnedArena(args.pinned_guard_gib << 30)
+        avail = mem_available_bytes() - (16 << 30)
+        needs += [b for b in (streamed_host_bytes(S, k, args) + PROBE_BYTES for k in streamed_keys)
+                  if b <= avail]
+        if args.streamed_arena == "hostalloc" and max(needs) > 0:
+            arena = PinnedArena(max(needs))
 
     st = S.slide_state_create([n], R, device=local)
     try:
@@ -721,13 +962,14 @@ def run_ours(args):
         e2e = None
         if not args.no_e2e:
             Ke = max(3, min(args.e2e_steps, K))
-            host_reps = [[torch.empty(n, dtype=torch.int16, pin_memory=True) for _ in range(R)] for _ in range(2)]
+            alloc = pinned_empty(torch, arena)
+            host_reps = [[alloc(n, torch.int16) for _ in range(R)] for _ in range(2)]
             for b in range(2):
                 for r in range(R):
                     host_reps[b][r].copy_(batches[b % len(batches)][r][:n])
             dev_reps = [[torch.empty(n + 64, dtype=torch.int16, device="cuda") for _ in range(R)] for _ in range(2)]
             out_dev = [torch.empty(n + 64, dtype=torch.int16, device="cuda") for _ in range(2)]
-            out_host = [torch.empty(n, dtype=torch.int16, pin_memory=True) for _ in range(2)]
+            out_host = [alloc(n, torch.int16) for _ in range(2)]
             copy_stream = torch.cuda.Stream()
             landed = [torch.cuda.Event() for _ in range(2)]
             consumed = [torch.cuda.Event() for _ in range(2)]
@@ -776,9 +1018,15 @@ def run_ours(args):
             e2e = {"value": n * Ke * world / (ms_e2e * 1e-3) / 1e9, "unit": UNIT,
                    "h2d_bytes_per_step": 2 * R * n, "d2h_bytes_per_step": 2 * n, "steps": Ke,
                    "pipelining": "copy-in of step k+1 on a copy stream overlaps step k's update and copy-out"}
+            del host_reps, out_host, dev_reps, out_dev
+            if arena is not None:
+                arena.reset()
     finally:
         S.slide_state_destroy(st)
 
+    del batches
+    release_pinned_cache(torch)
+    torch.cuda.empty_cache()
     variant = None
     cpu_route = None
     others = None
@@ -790,13 +1038,34 @@ def run_ours(args):
                                              max_steps=200 if name == "h5120_R8_logscale" else 500)
                   for name in W.HBM_RESIDENT if name != args.workload}
         import reduce_routes
-        cpu_route = reduce_routes.measure_cpu_reduce_route(S, torch, synth, n, R)
-    streamed = streamed_also = None
-    if not args.no_streamed and world == 1:
-        streamed = run_streamed(args, S, torch, synth, args.streamed_workload)
-        also = [x for x in args.streamed_also.split(",") if x and x != args.streamed_workload]
-        if also:
-            streamed_also = {x: run_streamed(args, S, torch, synth, x) for x in also}
+        # the host reduction reads and writes these buffers with the CPU, so
+        # they come from torch's pinned memory, not from the arena that the
+        # streamed states use (pinned pages the CPU has touched are read
+        # slowly by the copy engines for a while on these hosts)
+        # on the h2560 R = 4 layer (the headline layer's buffers would crowd the
+        # host next to the largest streamed leg's pinned state)
+        w_route = W.h2560_r4_clip()
+        cpu_route = reduce_routes.measure_cpu_reduce_route(S, torch, synth, w_route.units[0].numel, w_route.R)
+        cpu_route["workload"] = w_route.name
+    streamed = streamed_also = chunk_sweep = None
+    release_pinned_cache(torch)
+    try:
+        if streamed_keys:
+            streamed = run_streamed(args, S, torch, synth, args.streamed_workload, arena)
+            also = streamed_keys[1:]
+            if also:
+                streamed_also = {x: run_streamed(args, S, torch, synth, x, arena) for x in also}
+            if args.chunk_sweep and arena is not None and "link" in streamed:
+                pts = [tuple(int(v) for v in p.split(":")) for p in args.chunk_sweep.split(",")]
+                chunk_sweep = {}
+                for key in [k for k in args.chunk_sweep_workloads.split(",") if k]:
+                    if streamed_host_bytes(S, key, args) <= arena.nbytes:
+                        chunk_sweep[key] = run_chunk_sweep(args, S, torch, synth, key, arena, streamed["link"], pts)
+    finally:
+        if arena is not None:
+            arena.free()
+        if guard is not None:
+            guard.free()
 
     if rank != 0:
         if dist:
@@ -864,6 +1133,7 @@ def run_ours(args):
         "cpu_reduce_route": cpu_route,
         "streamed": streamed,
         "streamed_also": streamed_also,
+        "chunk_sweep": chunk_sweep,
     }
     report(line, args.detail_out)
     if dist:
@@ -975,13 +1245,15 @@ def compact_headline(full):
         line["streamed"] = st
     cr = full.get("cpu_reduce_route")
     if cr:
-        line["cpu_reduce_route"] = {"cpu_route_s": _r(cr["cpu_route"]["s"]), "gpu_route_s": _r(cr["gpu_route"]["s"]),
+        line["cpu_reduce_route"] = {"workload": cr.get("workload"),
+                                    "cpu_route_s": _r(cr["cpu_route"]["s"]), "gpu_route_s": _r(cr["gpu_route"]["s"]),
                                     "cpu_route_d2h_bytes": cr["cpu_route"]["d2h_bytes"],
                                     "identical_results": cr["identical_results"]}
     sw = full.get("chunk_sweep")
     if sw:
-        line["chunk_sweep"] = {"workload": sw["workload"], "chosen": sw.get("chosen"),
-                               "points": [[p["h2d_mib"], p["d2h_mib"], _r(p["frac"])] for p in sw["points"]]}
+        line["chunk_sweep"] = {k: {"chosen": v.get("chosen"),
+                                   "points": [[p["h2d_mib"], p["d2h_mib"], _r(p["frac"], 3)] for p in v["points"]]}
+                               for k, v in sw.items()}
     return line
 
 

@@ -67,7 +67,7 @@ extern "C" {
 /* Same type as cudaStream_t, declared without the CUDA headers. */
 typedef struct CUstream_st *slide_stream_t;
 
-#define SLIDE_ABI_VERSION 1
+#define SLIDE_ABI_VERSION 2
 #define SLIDE_MAX_REPLICAS 8
 
 typedef enum {
@@ -97,13 +97,18 @@ enum {
     SLIDE_FLAG_FP32_GRADS = 4u,          /* the R gradient replicas are FP32 (FP32 gradient
                                             accumulation), not BF16: every replica pointer then holds
                                             n floats, and the step moves 26 + 4R bytes per parameter */
-    SLIDE_FLAG_BF16_COPY_IN_HBM = 8u     /* streamed residency: keep the BF16 compute copy in HBM
+    SLIDE_FLAG_BF16_COPY_IN_HBM = 8u,    /* streamed residency: keep the BF16 compute copy in HBM
                                             (2 B/param of device memory) instead of the pinned host
                                             mirror; the host holds 12 B/param and the link carries
                                             12 B/param each way per step (the update writes each
                                             unit's resident copy in place: the copy is neither
                                             delivered nor written back, and the window has no BF16
                                             buffers) */
+    SLIDE_FLAG_HOST_HUGE_PAGES = 16u     /* streamed residency: back the pinned host state with an
+                                            anonymous mapping advised for transparent huge pages and
+                                            pinned with cudaHostRegister, instead of cudaHostAlloc
+                                            (physically contiguous where the host kernel can provide
+                                            it; the mapping is rounded up to the huge page size) */
 };
 
 /* Adam hyper-parameters (FP32).  Valid: lr >= 0, 0 <= beta1 < 1,
@@ -123,7 +128,17 @@ typedef struct {
     int32_t device;              /* CUDA device ordinal */
     uint32_t timeout_ms;         /* streamed: bound of each host wait (0 = 600000) */
     uint32_t flags;              /* SLIDE_FLAG_* */
-    int64_t chunk_bytes;         /* streamed: copy chunk (0 = 64 MiB); multiple of 256 */
+    int64_t chunk_bytes;         /* streamed: host->device chunk of master, m and v, and the
+                                    update's chunk (0 = 64 MiB); bytes of FP32, multiple of 256 */
+    int64_t chunk_bytes_d2h;     /* streamed: device->host write-back chunk (0 = chunk_bytes);
+                                    bytes of FP32, multiple of 256 */
+    void *host_arena;            /* streamed: caller-owned pinned host memory (cudaHostAlloc, or
+                                    cudaHostRegister with cudaHostRegisterMapped), 256-byte
+                                    aligned, to hold the host state instead of an allocation of
+                                    the state's own; NULL = the state allocates it.  The state
+                                    zeroes and uses the first host_pinned_bytes (slide_state_bytes)
+                                    and never frees it; it must outlive the state. */
+    int64_t host_arena_bytes;    /* size of host_arena in bytes (>= the state's host bytes) */
 } slide_config;
 
 typedef struct slide_state slide_state; /* opaque; owns all of its memory */
@@ -141,8 +156,12 @@ typedef int (*slide_grad_fn)(void *user, int32_t layer, void *const *replica_dev
 
 /* Create a state: allocates master, m, v, the BF16 copy (all zero, t = 0) and
  * the per-layer device scratch of the clip reduction; for the streamed
- * residency also the pinned host state, the 2-slot HBM window and the copy
- * and compute streams.  *out is set only on SLIDE_OK.
+ * residency also the pinned host state (or uses the caller's host_arena), the
+ * 2-slot HBM window and the copy and compute streams.  *out is set only on
+ * SLIDE_OK.  A caller that creates streamed states one after another can pin
+ * one arena once and hand it to each: on the GB300 hosts measured, pinning and
+ * freeing 100+ GB repeatedly left later pinned allocations with regions that
+ * the copy engines read several times slower.
  * Defined by: "SlideDP: Scaling Host-Resident LLM Fine-Tuning Across Multiple
  * GPUs", Prerequisites (the 16N-byte state of mixed-precision Adam) and Core
  * method (one authoritative FP32 master and (m_l, v_l) per layer, held on the
@@ -349,12 +368,16 @@ SLIDE_API slide_status slide_deliver_bf16(slide_state *st, int32_t layer, void *
 
 /* Timeline of the last slide_model_step_streamed, for tracing how the copies
  * and the updates overlap (host-streamed residency).  out receives, for each
- * unit l, 6 values in milliseconds from the start of that step:
- *   [6l+0] copy-in of master/m/v began   [6l+1] master landed
- *   [6l+2] copy-in ended                 [6l+3] update kernel ended
- *   [6l+4] write-back began              [6l+5] write-back ended
- * and out[6L] = end of the forward sweep (BF16 delivery); NaN where a unit
- * did not get that far.  cap = number of doubles in out (>= 6L + 1).
+ * unit l, 8 values in milliseconds from the start of that step:
+ *   [8l+0] copy-in of master/m/v began   [8l+1] master landed
+ *   [8l+2] copy-in ended                 [8l+3] update kernel ended
+ *   [8l+4] write-back began              [8l+5] write-back ended
+ * (from events on the device), and, by the host clock from the moment the
+ * step's first operation was enqueued,
+ *   [8l+6] the copy-in of l was fully enqueued
+ *   [8l+7] the update and write-back of l were fully enqueued;
+ * and out[8L] = end of the forward sweep (BF16 delivery); NaN where a unit
+ * did not get that far.  cap = number of doubles in out (>= 8L + 1).
  * Defined by: "SlideDP: Scaling Host-Resident LLM Fine-Tuning Across Multiple
  * GPUs", Core method and its figure on the chunked pipeline (how the copies
  * in, the update and the copies out of a layer overlap). */

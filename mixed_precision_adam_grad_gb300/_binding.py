@@ -37,6 +37,7 @@ SLIDE_FLAG_CHECK_FINITE = 1
 SLIDE_FLAG_TEST_PIPELINE_STALL = 2
 SLIDE_FLAG_FP32_GRADS = 4
 SLIDE_FLAG_BF16_COPY_IN_HBM = 8
+SLIDE_FLAG_HOST_HUGE_PAGES = 16
 SLIDE_MAX_REPLICAS = 8
 SLIDE_DELIVER_FULL = 0
 SLIDE_DELIVER_SHARDED = 1
@@ -57,7 +58,8 @@ class slide_config(C.Structure):
     _fields_ = [("n_layers", C.c_int32), ("layer_numel", C.POINTER(C.c_int64)),
                 ("n_replicas", C.c_int32), ("residency", C.c_int32),
                 ("window_layers", C.c_int32), ("device", C.c_int32),
-                ("timeout_ms", C.c_uint32), ("flags", C.c_uint32), ("chunk_bytes", C.c_int64)]
+                ("timeout_ms", C.c_uint32), ("flags", C.c_uint32), ("chunk_bytes", C.c_int64),
+                ("chunk_bytes_d2h", C.c_int64), ("host_arena", C.c_void_p), ("host_arena_bytes", C.c_int64)]
 
 
 SLIDE_GRAD_FN = C.CFUNCTYPE(C.c_int, C.c_void_p, C.c_int32, C.POINTER(C.c_void_p), C.c_void_p)
@@ -155,10 +157,11 @@ def hparams(lr=1e-5, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, max_gr
 
 
 def _config(layer_numel: Sequence[int], n_replicas: int, residency: int, device: int,
-            flags: int, timeout_ms: int, chunk_bytes: int, window_layers: int):
+            flags: int, timeout_ms: int, chunk_bytes: int, window_layers: int, chunk_bytes_d2h: int = 0,
+            host_arena=None, host_arena_bytes: int = 0):
     arr = (C.c_int64 * len(layer_numel))(*[int(n) for n in layer_numel])
     cfg = slide_config(len(layer_numel), arr, n_replicas, residency, window_layers, device,
-                       timeout_ms, flags, chunk_bytes)
+                       timeout_ms, flags, chunk_bytes, chunk_bytes_d2h, _ptr(host_arena), host_arena_bytes)
     cfg._keep = arr
     return cfg
 
@@ -192,16 +195,23 @@ def slide_last_error() -> str:
 
 
 def slide_state_bytes(layer_numel, n_replicas, residency=SLIDE_RESIDENCY_HBM, device=0, flags=0,
-                      timeout_ms=0, chunk_bytes=0, window_layers=2):
-    cfg = _config(layer_numel, n_replicas, residency, device, flags, timeout_ms, chunk_bytes, window_layers)
+                      timeout_ms=0, chunk_bytes=0, window_layers=2, chunk_bytes_d2h=0, host_arena=None,
+                      host_arena_bytes=0):
+    cfg = _config(layer_numel, n_replicas, residency, device, flags, timeout_ms, chunk_bytes, window_layers,
+                  chunk_bytes_d2h, host_arena, host_arena_bytes)
     dev, host = C.c_int64(), C.c_int64()
     _check(_lib().slide_state_bytes(C.byref(cfg), C.byref(dev), C.byref(host)))
     return dev.value, host.value
 
 
 def slide_state_create(layer_numel, n_replicas, residency=SLIDE_RESIDENCY_HBM, device=0, flags=0,
-                       timeout_ms=0, chunk_bytes=0, window_layers=2) -> SlideState:
-    cfg = _config(layer_numel, n_replicas, residency, device, flags, timeout_ms, chunk_bytes, window_layers)
+                       timeout_ms=0, chunk_bytes=0, window_layers=2, chunk_bytes_d2h=0, host_arena=None,
+                       host_arena_bytes=0) -> SlideState:
+    """host_arena: caller-owned pinned host memory (an address, or a pinned
+    tensor) of host_arena_bytes bytes for the streamed state; it must outlive
+    the state."""
+    cfg = _config(layer_numel, n_replicas, residency, device, flags, timeout_ms, chunk_bytes, window_layers,
+                  chunk_bytes_d2h, host_arena, host_arena_bytes)
     out = C.c_void_p()
     _check(_lib().slide_state_create(C.byref(cfg), C.byref(out)))
     return SlideState(out.value, layer_numel, n_replicas, residency)
@@ -305,11 +315,12 @@ def slide_streamed_timeline(st: SlideState):
     """Per-unit timeline (ms) of the last streamed step: a list of dicts and
     the end of the forward sweep."""
     L = len(st.layer_numel)
-    buf = (C.c_double * (6 * L + 1))()
-    _check(_lib().slide_streamed_timeline(C.c_void_p(st.handle), buf, 6 * L + 1))
-    keys = ("h2d_begin", "master_landed", "h2d_end", "update_end", "d2h_begin", "d2h_end")
-    units = [dict(zip(keys, buf[6 * l:6 * l + 6])) for l in range(L)]
-    return units, buf[6 * L]
+    buf = (C.c_double * (8 * L + 1))()
+    _check(_lib().slide_streamed_timeline(C.c_void_p(st.handle), buf, 8 * L + 1))
+    keys = ("h2d_begin", "master_landed", "h2d_end", "update_end", "d2h_begin", "d2h_end",
+            "host_copyin_enqueued", "host_unit_enqueued")
+    units = [dict(zip(keys, buf[8 * l:8 * l + 8])) for l in range(L)]
+    return units, buf[8 * L]
 
 
 def slide_deliver_bf16(st: SlideState, layer: int, dst, route=SLIDE_DELIVER_FULL, stream=None) -> None:

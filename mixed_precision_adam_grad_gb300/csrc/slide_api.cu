@@ -12,6 +12,8 @@
 // step path).
 #include <cuda_runtime.h>
 
+#include <sys/mman.h>
+
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -94,8 +96,20 @@ static slide_status check_config(const slide_config *cfg, int64_t *max_numel)
         return fail(SLIDE_ERR_INVALID_ARG, "config: window_layers must be 2 (or 0 for the default 2)");
     if (cfg->chunk_bytes < 0 || (cfg->chunk_bytes % 256) != 0)
         return fail(SLIDE_ERR_INVALID_ARG, "config: chunk_bytes must be a non-negative multiple of 256");
+    if (cfg->chunk_bytes_d2h < 0 || (cfg->chunk_bytes_d2h % 256) != 0)
+        return fail(SLIDE_ERR_INVALID_ARG, "config: chunk_bytes_d2h must be a non-negative multiple of 256");
+    if (cfg->host_arena) {
+        if (cfg->residency != SLIDE_RESIDENCY_HOST_STREAMED)
+            return fail(SLIDE_ERR_INVALID_ARG, "config: host_arena is for the streamed residency only");
+        if (((uintptr_t)cfg->host_arena & 255u) != 0)
+            return fail(SLIDE_ERR_INVALID_ARG, "config: host_arena must be 256-byte aligned");
+        if (cfg->flags & SLIDE_FLAG_HOST_HUGE_PAGES)
+            return fail(SLIDE_ERR_INVALID_ARG, "config: host_arena and SLIDE_FLAG_HOST_HUGE_PAGES exclude each other");
+    } else if (cfg->host_arena_bytes != 0) {
+        return fail(SLIDE_ERR_INVALID_ARG, "config: host_arena_bytes without a host_arena");
+    }
     if (cfg->flags & ~(uint32_t)(SLIDE_FLAG_CHECK_FINITE | SLIDE_FLAG_TEST_PIPELINE_STALL | SLIDE_FLAG_FP32_GRADS |
-                                 SLIDE_FLAG_BF16_COPY_IN_HBM))
+                                 SLIDE_FLAG_BF16_COPY_IN_HBM | SLIDE_FLAG_HOST_HUGE_PAGES))
         return fail(SLIDE_ERR_INVALID_ARG, "config: unknown flag bits");
     if (cfg->device < 0)
         return fail(SLIDE_ERR_INVALID_ARG, "config: device < 0");
@@ -164,6 +178,76 @@ slide_status slide_state_bytes(const slide_config *cfg, int64_t *device_bytes, i
     return SLIDE_OK;
 }
 
+// Size of a transparent huge page on this host (the PMD size), 2 MiB if the
+// kernel does not say.
+static size_t huge_page_bytes()
+{
+    size_t hp = 0;
+    if (FILE *f = fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r")) {
+        unsigned long long v = 0;
+        if (fscanf(f, "%llu", &v) == 1)
+            hp = (size_t)v;
+        fclose(f);
+    }
+    return (hp >= 4096 && (hp & (hp - 1)) == 0) ? hp : ((size_t)2 << 20);
+}
+
+// The pinned host arena.  Default: cudaHostAlloc.  With
+// SLIDE_FLAG_HOST_HUGE_PAGES: an anonymous mapping aligned to the huge page
+// size, advised MADV_HUGEPAGE before its pages are touched, then pinned and
+// mapped for the device with cudaHostRegister (which faults the pages in), so
+// the arena is backed by physically contiguous huge pages where the kernel
+// can provide them.
+static cudaError_t host_arena_alloc(slide_state *st, size_t bytes)
+{
+    if (st->cfg.host_arena) {  // the caller's pinned memory, checked by the caller of this function
+        st->host_arena = st->cfg.host_arena;
+        st->host_arena_owned = false;
+        return cudaSuccess;
+    }
+    st->host_arena_owned = true;
+    if (!(st->cfg.flags & SLIDE_FLAG_HOST_HUGE_PAGES))
+        return cudaHostAlloc(&st->host_arena, bytes > 0 ? bytes : 1, cudaHostAllocDefault);
+    const size_t hp = huge_page_bytes();
+    const size_t len = (bytes + hp - 1) / hp * hp + (bytes == 0 ? hp : 0);
+    void *raw = mmap(nullptr, len + hp, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS | MAP_NORESERVE, -1, 0);
+    if (raw == MAP_FAILED)
+        return cudaErrorMemoryAllocation;
+    const uintptr_t a = ((uintptr_t)raw + hp - 1) & ~(uintptr_t)(hp - 1);
+    const size_t head = a - (uintptr_t)raw;
+    if (head)
+        munmap(raw, head);
+    if (hp - head)
+        munmap((char *)a + len, hp - head);
+    madvise((void *)a, len, MADV_HUGEPAGE);
+    cudaError_t e = cudaHostRegister((void *)a, len, cudaHostRegisterPortable | cudaHostRegisterMapped);
+    if (e != cudaSuccess) {
+        munmap((void *)a, len);
+        return e;
+    }
+    st->host_arena = (void *)a;
+    st->host_map_bytes = len;
+    return cudaSuccess;
+}
+
+static void host_arena_free(slide_state *st)
+{
+    if (!st->host_arena)
+        return;
+    if (!st->host_arena_owned) {
+        st->host_arena = nullptr;
+        return;
+    }
+    if (st->host_map_bytes) {
+        cudaHostUnregister(st->host_arena);
+        munmap(st->host_arena, st->host_map_bytes);
+    } else {
+        cudaFreeHost(st->host_arena);
+    }
+    st->host_arena = nullptr;
+    st->host_map_bytes = 0;
+}
+
 slide_status slide_state_create(const slide_config *cfg, slide_state **out)
 {
     if (!out)
@@ -193,6 +277,8 @@ slide_status slide_state_create(const slide_config *cfg, slide_state **out)
         st->cfg.timeout_ms = 600000;
     if (st->cfg.chunk_bytes == 0)
         st->cfg.chunk_bytes = (int64_t)64 << 20;
+    if (st->cfg.chunk_bytes_d2h == 0)
+        st->cfg.chunk_bytes_d2h = st->cfg.chunk_bytes;
     st->device = cfg->device;
     st->numel.assign(cfg->layer_numel, cfg->layer_numel + cfg->n_layers);
     st->layers.resize(cfg->n_layers);
@@ -239,12 +325,28 @@ slide_status slide_state_create(const slide_config *cfg, slide_state **out)
             }
         }
         st->host_bytes = state_bytes;
-        e = cudaHostAlloc(&st->host_arena, st->host_bytes > 0 ? st->host_bytes : 1, cudaHostAllocDefault);
+        if (cfg->host_arena) {
+            // the caller's arena must be large enough and pinned host memory
+            cudaPointerAttributes pa{};
+            const bool pinned = cudaPointerGetAttributes(&pa, cfg->host_arena) == cudaSuccess &&
+                                pa.type == cudaMemoryTypeHost;
+            cudaGetLastError();
+            const char *why = cfg->host_arena_bytes < (int64_t)state_bytes
+                                  ? "config: host_arena_bytes is smaller than the state's host bytes"
+                                  : (!pinned ? "config: host_arena is not pinned (page-locked) host memory" : nullptr);
+            if (why) {
+                if (st->dev_arena)
+                    cudaFree(st->dev_arena);
+                delete st;
+                return fail(SLIDE_ERR_INVALID_ARG, why);
+            }
+        }
+        e = host_arena_alloc(st, st->host_bytes);
         if (e != cudaSuccess || getenv("SLIDE_FAULT_PINNED_ALLOC")) {
             // SLIDE_FAULT_PINNED_ALLOC injects this failure for tests of the
             // clean-up path (nothing stays allocated).
             if (e == cudaSuccess)
-                cudaFreeHost(st->host_arena);
+                host_arena_free(st);
             cudaGetLastError();
             if (st->dev_arena)
                 cudaFree(st->dev_arena);
@@ -298,7 +400,7 @@ slide_status slide_state_create(const slide_config *cfg, slide_state **out)
     } else {
         rc = engine_create(st);
         if (rc != SLIDE_OK) {
-            cudaFreeHost(st->host_arena);
+            host_arena_free(st);
             if (st->dev_arena)
                 cudaFree(st->dev_arena);
             delete st;
@@ -321,8 +423,7 @@ void slide_state_destroy(slide_state *st)
         cudaDeviceSynchronize();
         cudaFree(st->dev_arena);
     }
-    if (st->host_arena)
-        cudaFreeHost(st->host_arena);
+    host_arena_free(st);
     delete st;
 }
 
@@ -403,6 +504,38 @@ static void refresh_aborted(slide_state *st)
     st->aborted = false;
 }
 
+// Copy `bytes` between caller memory and the state's arrays.  For the pinned
+// host state of the streamed residency the copy goes through a device buffer
+// of the window, so that only DMA touches the pinned state: on the GB300
+// hosts measured, pinned pages that the CPU had read or written were read
+// several times slower by the copy engines for a while afterwards, and a
+// host-to-host cudaMemcpy is a CPU copy.
+static cudaError_t state_copy(slide_state *st, void *dst, const void *src, size_t bytes, bool to_state)
+{
+    if (bytes == 0)
+        return cudaSuccess;
+    if (st->cfg.residency != SLIDE_RESIDENCY_HOST_STREAMED)
+        return cudaMemcpy(dst, src, bytes, cudaMemcpyDefault);
+    cudaPointerAttributes pa{};
+    const void *state_side = to_state ? dst : src;
+    if (cudaPointerGetAttributes(&pa, state_side) != cudaSuccess || pa.type != cudaMemoryTypeHost) {
+        cudaGetLastError();  // device-resident (the BF16 copy kept in HBM)
+        return cudaMemcpy(dst, src, bytes, cudaMemcpyDefault);
+    }
+    size_t cap = 0;
+    char *stage = (char *)engine_staging(st, &cap);
+    if (!stage || cap == 0)
+        return cudaMemcpy(dst, src, bytes, cudaMemcpyDefault);
+    cudaError_t e = cudaSuccess;
+    for (size_t off = 0; off < bytes && e == cudaSuccess; off += cap) {
+        const size_t len = bytes - off < cap ? bytes - off : cap;
+        e = cudaMemcpy(stage, (const char *)src + off, len, cudaMemcpyDefault);
+        if (e == cudaSuccess)
+            e = cudaMemcpy((char *)dst + off, stage, len, cudaMemcpyDefault);
+    }
+    return e;
+}
+
 slide_status slide_layer_set(slide_state *st, int32_t layer, const float *master, const float *m,
                              const float *v, int64_t step)
 {
@@ -424,7 +557,7 @@ slide_status slide_layer_set(slide_state *st, int32_t layer, const float *master
     for (int k = 0; k < 3; ++k) {
         if (!src[k] || bytes == 0)
             continue;
-        e = cudaMemcpy(dst[k], src[k], bytes, cudaMemcpyDefault);
+        e = state_copy(st, dst[k], src[k], bytes, true);
         if (e != cudaSuccess)
             return fail_cuda(e, "cudaMemcpy in slide_layer_set");
     }
@@ -471,7 +604,7 @@ slide_status slide_layer_get(slide_state *st, int32_t layer, float *master, floa
     for (int k = 0; k < 4; ++k) {
         if (!dst[k] || bytes[k] == 0)
             continue;
-        e = cudaMemcpy(dst[k], src[k], bytes[k], cudaMemcpyDefault);
+        e = state_copy(st, dst[k], src[k], bytes[k], false);
         if (e != cudaSuccess)
             return fail_cuda(e, "cudaMemcpy in slide_layer_get");
     }

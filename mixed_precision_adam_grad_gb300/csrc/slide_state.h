@@ -49,8 +49,10 @@ struct slide_state {
     int device = 0;
     void *dev_arena = nullptr;   // one cudaMalloc for all device arrays
     size_t dev_bytes = 0;
-    void *host_arena = nullptr;  // one cudaHostAlloc (streamed residency)
+    void *host_arena = nullptr;  // pinned host state (streamed residency)
     size_t host_bytes = 0;
+    size_t host_map_bytes = 0;   // > 0: host_arena is a registered mapping of this length (huge pages)
+    bool host_arena_owned = true;  // false: host_arena is the caller's (never freed here)
     slide::StreamEngine *engine = nullptr;
     bool aborted = false;
     cudaEvent_t trace[3] = {nullptr, nullptr, nullptr};  // prepass start, update start, update stop
@@ -78,5 +80,8 @@ void engine_destroy(slide_state *st);
 size_t engine_device_bytes(const slide_config &cfg, int64_t max_numel);
 slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const slide_adam_hparams &hp);
 slide_status engine_timeline(slide_state *st, double *out, int64_t cap);
+// A device buffer of the window (idle between steps) of *capacity bytes, for
+// moving data between caller memory and the pinned state by DMA only.
+void *engine_staging(slide_state *st, size_t *capacity);
 
 }  // namespace slide

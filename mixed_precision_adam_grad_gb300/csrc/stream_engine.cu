@@ -31,9 +31,15 @@
 // writes the unit's resident copy in place, there is nothing to deliver or
 // write back, and the link carries 12 B each way.
 //
-// A unit's arrays are split into chunks of chunk_bytes of FP32 (the BF16
-// copy and the replicas use the same element ranges).  Schedule of one step,
-// all enqueued up front, then one bounded host wait per stream:
+// A unit's arrays are split into copy-in chunks of chunk_bytes of FP32 (the
+// granule of the host-to-device copies of master, m and v and of the update)
+// and write-back chunks of chunk_bytes_d2h of FP32 (the granule of the
+// device-to-host copies); the BF16 copy and the replicas use the same element
+// ranges.  A copy into bytes of a slot waits for every write-back chunk that
+// overlaps them, and a write-back chunk waits for the last update chunk that
+// overlaps it (each stream runs in order, so these waits cover everything
+// earlier).  Schedule of one step, all enqueued up front, then one bounded
+// host wait per stream:
 //  forward sweep (H2D stream): the BF16 copy of unit l -> slot l%2, in order
 //                  (skipped when the copy is kept in HBM);
 //  reverse sweep, l = L-1 .. 0, slot s = l%2:
@@ -76,9 +82,9 @@ struct Slot {
     void *g[kMaxReplicas] = {};
     ClipScratch scratch{};
     // chunk k of region r has been written back by the unit that used this slot last
-    std::vector<cudaEvent_t> freed[kRegions];
-    std::vector<cudaEvent_t> mv_landed;  // chunk k of m and v has arrived
-    std::vector<cudaEvent_t> upd_done;   // chunk k has been updated
+    std::vector<cudaEvent_t> freed[kRegions];  // per write-back chunk
+    std::vector<cudaEvent_t> mv_landed;  // copy-in chunk k of m and v has arrived
+    std::vector<cudaEvent_t> upd_done;   // copy-in chunk k has been updated
 };
 
 size_t grad_bytes(const slide_config &cfg) { return (cfg.flags & SLIDE_FLAG_FP32_GRADS) ? 4 : 2; }
@@ -103,13 +109,18 @@ struct StreamEngine {
     void *window = nullptr;
     size_t window_bytes = 0;
     Slot slots[kSlots];
-    int64_t chunk_elems = 0;  // parameters per chunk
-    int max_chunks = 0;
+    int64_t chunk_elems = 0;  // parameters per copy-in (and update) chunk
+    int64_t out_elems = 0;    // parameters per write-back chunk
+    int max_chunks = 0;       // copy-in chunks of the largest unit
+    int max_out = 0;          // write-back chunks of the largest unit
     size_t gsize = 2;         // bytes per gradient value
     cudaStream_t s_h2d = nullptr, s_comp = nullptr, s_d2h = nullptr;
     // per unit, timing events (also the timeline of the last step)
     std::vector<cudaEvent_t> h2d_begin, theta_done, h2d_done, kern_done, d2h_begin, d2h_end;
     std::vector<char> recorded;  // unit reached its write-back in the last step
+    // host clock (ms since the step's first event was enqueued) at which the
+    // copy-in of unit l, and its update and write-back, were fully enqueued
+    std::vector<double> host_copyin_enqueued, host_unit_enqueued;
     cudaEvent_t step_start = nullptr, fwd_done = nullptr;
     cudaEvent_t sweep_done[3] = {nullptr, nullptr, nullptr};  // end of the H2D, compute, D2H streams
 
@@ -120,6 +131,25 @@ struct StreamEngine {
         return {off, len};
     }
     int n_chunks(int64_t n) const { return (int)((n + chunk_elems - 1) / chunk_elems); }
+    Chunk out_chunk(int64_t n, int q) const
+    {
+        const int64_t off = (int64_t)q * out_elems;
+        const int64_t len = n - off < out_elems ? n - off : out_elems;
+        return {off, len};
+    }
+    int n_out(int64_t n) const { return (int)((n + out_elems - 1) / out_elems); }
+    // make `stream` wait until every write-back chunk of `region` of slot s
+    // that overlaps elements [c.off, c.off + c.len) has completed
+    cudaError_t wait_freed(cudaStream_t stream, const Slot &s, int region, const Chunk &c) const
+    {
+        cudaError_t e = cudaSuccess;
+        if (c.len <= 0)
+            return e;
+        const int q0 = (int)(c.off / out_elems), q1 = (int)((c.off + c.len - 1) / out_elems);
+        for (int q = q0; q <= q1 && e == cudaSuccess; ++q)
+            e = cudaStreamWaitEvent(stream, s.freed[region][q], 0);
+        return e;
+    }
 };
 
 size_t engine_device_bytes(const slide_config &cfg, int64_t max_numel)
@@ -163,8 +193,10 @@ slide_status engine_create(slide_state *st)
         maxn = n > maxn ? n : maxn;
     const int R = st->cfg.n_replicas;
     E->gsize = grad_bytes(st->cfg);
-    E->chunk_elems = st->cfg.chunk_bytes / 4;  // chunk_bytes is a positive multiple of 256
+    E->chunk_elems = st->cfg.chunk_bytes / 4;  // chunk sizes are positive multiples of 256
+    E->out_elems = st->cfg.chunk_bytes_d2h / 4;
     E->max_chunks = E->n_chunks(maxn);
+    E->max_out = E->n_out(maxn);
     E->window_bytes = engine_device_bytes(st->cfg, maxn);
     cudaError_t e = cudaMalloc(&E->window, E->window_bytes);
     if (e != cudaSuccess) {
@@ -194,16 +226,16 @@ slide_status engine_create(slide_state *st)
         s.scratch.coef = (float *)(p + align_up(sizeof(double) * kMaxPartials));
         s.scratch.status = (unsigned *)(s.scratch.coef + 1);
         p += scratch_bytes();
-        auto make = [&](std::vector<cudaEvent_t> &v) {
-            v.assign(E->max_chunks, nullptr);
+        auto make = [&](std::vector<cudaEvent_t> &v, int count) {
+            v.assign(count, nullptr);
             for (auto &ev : v)
                 if (e == cudaSuccess)
                     e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
         };
         for (auto &v : s.freed)
-            make(v);
-        make(s.mv_landed);
-        make(s.upd_done);
+            make(v, E->max_out);
+        make(s.mv_landed, E->max_chunks);
+        make(s.upd_done, E->max_chunks);
     }
     const size_t L = st->layers.size();
     for (auto *v : {&E->h2d_begin, &E->theta_done, &E->h2d_done, &E->kern_done, &E->d2h_begin, &E->d2h_end}) {
@@ -213,6 +245,8 @@ slide_status engine_create(slide_state *st)
                 e = cudaEventCreate(&ev);
     }
     E->recorded.assign(L, 0);
+    E->host_copyin_enqueued.assign(L, __builtin_nan(""));
+    E->host_unit_enqueued.assign(L, __builtin_nan(""));
     if (e == cudaSuccess)
         e = cudaEventCreate(&E->step_start);
     if (e == cudaSuccess)
@@ -240,6 +274,20 @@ slide_status engine_create(slide_state *st)
     st->engine = E;
     st->dev_bytes = E->window_bytes;
     return SLIDE_OK;
+}
+
+void *engine_staging(slide_state *st, size_t *capacity)
+{
+    StreamEngine *E = st->engine;
+    if (!E) {
+        *capacity = 0;
+        return nullptr;
+    }
+    int64_t maxn = 0;
+    for (int64_t n : st->numel)
+        maxn = n > maxn ? n : maxn;
+    *capacity = (size_t)maxn * 4;
+    return E->slots[0].arr[0];
 }
 
 void engine_destroy(slide_state *st)
@@ -291,8 +339,10 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
     slide_status rc = SLIDE_OK;
     int done_units = 0;  // units whose update and write-back were enqueued (from L-1 down)
 
-    for (int l = 0; l < L; ++l)
+    for (int l = 0; l < L; ++l) {
         E->recorded[l] = 0;
+        E->host_copyin_enqueued[l] = E->host_unit_enqueued[l] = __builtin_nan("");
+    }
     // Profiler ranges (host side: when each part was enqueued): the step, and
     // each unit of the reverse sweep.  No effect without a profiler attached.
     struct Range {
@@ -300,6 +350,10 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
         ~Range() { nvtxRangePop(); }
     } step_range("slide streamed step t=" + std::to_string(t));
     e = cudaEventRecord(E->step_start, E->s_h2d);
+    const auto host_t0 = std::chrono::steady_clock::now();
+    auto host_ms = [&]() {
+        return std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - host_t0).count();
+    };
 
     // forward sweep: deliver the BF16 copy of every unit, in order (a copy
     // kept in HBM is already where the forward pass reads it)
@@ -308,7 +362,7 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
         const LayerState &U = st->layers[l];
         for (int k = 0; k < E->n_chunks(U.n) && e == cudaSuccess; ++k) {
             const Chunk c = E->chunk(U.n, k);
-            e = cudaStreamWaitEvent(E->s_h2d, s.freed[kW][k], 0);
+            e = E->wait_freed(E->s_h2d, s, kW, c);
             if (e == cudaSuccess)
                 e = cudaMemcpyAsync(s.w + c.off, U.w + c.off, (size_t)c.len * 2, cudaMemcpyHostToDevice,
                                     E->s_h2d);
@@ -325,7 +379,7 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
         cudaError_t err = cudaEventRecord(E->h2d_begin[l], E->s_h2d);
         for (int k = 0; k < K && err == cudaSuccess; ++k) {
             const Chunk c = E->chunk(U.n, k);
-            err = cudaStreamWaitEvent(E->s_h2d, s.freed[kTheta][k], 0);
+            err = E->wait_freed(E->s_h2d, s, kTheta, c);
             if (err == cudaSuccess)
                 err = cudaMemcpyAsync(s.arr[0] + c.off, U.theta + c.off, (size_t)c.len * 4,
                                       cudaMemcpyHostToDevice, E->s_h2d);
@@ -334,12 +388,12 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
             err = cudaEventRecord(E->theta_done[l], E->s_h2d);
         for (int k = 0; k < K && err == cudaSuccess; ++k) {
             const Chunk c = E->chunk(U.n, k);
-            err = cudaStreamWaitEvent(E->s_h2d, s.freed[kM][k], 0);
+            err = E->wait_freed(E->s_h2d, s, kM, c);
             if (err == cudaSuccess)
                 err = cudaMemcpyAsync(s.arr[1] + c.off, U.m + c.off, (size_t)c.len * 4, cudaMemcpyHostToDevice,
                                       E->s_h2d);
             if (err == cudaSuccess)
-                err = cudaStreamWaitEvent(E->s_h2d, s.freed[kV][k], 0);
+                err = E->wait_freed(E->s_h2d, s, kV, c);
             if (err == cudaSuccess)
                 err = cudaMemcpyAsync(s.arr[2] + c.off, U.v + c.off, (size_t)c.len * 4, cudaMemcpyHostToDevice,
                                       E->s_h2d);
@@ -348,6 +402,7 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
         }
         if (err == cudaSuccess)
             err = cudaEventRecord(E->h2d_done[l], E->s_h2d);
+        E->host_copyin_enqueued[l] = host_ms();
         return err;
     };
 
@@ -395,7 +450,7 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
             const Chunk c = E->chunk(U.n, k);
             e = cudaStreamWaitEvent(E->s_comp, s.mv_landed[k], 0);
             if (e == cudaSuccess && w_slot)
-                e = cudaStreamWaitEvent(E->s_comp, s.freed[kW][k], 0);
+                e = E->wait_freed(E->s_comp, s, kW, c);
             if (e != cudaSuccess)
                 break;
             ReplicaPtrs gk{};
@@ -412,23 +467,26 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
             e = cudaEventRecord(E->kern_done[l], E->s_comp);
         if (e != cudaSuccess)
             break;
-        // write-back of l, chunk by chunk behind its update
+        // write-back of l, chunk by chunk behind its update: write-back chunk q
+        // waits for the last update chunk that overlaps it
         float *dst[3] = {U.theta, U.m, U.v};
-        for (int k = 0; k < K && e == cudaSuccess; ++k) {
-            const Chunk c = E->chunk(U.n, k);
-            e = cudaStreamWaitEvent(E->s_d2h, s.upd_done[k], 0);
-            if (e == cudaSuccess && k == 0)
+        const int Q = E->n_out(U.n);
+        for (int q = 0; q < Q && e == cudaSuccess; ++q) {
+            const Chunk c = E->out_chunk(U.n, q);
+            const int k_last = (int)((c.off + c.len - 1) / E->chunk_elems);
+            e = cudaStreamWaitEvent(E->s_d2h, s.upd_done[k_last], 0);
+            if (e == cudaSuccess && q == 0)
                 e = cudaEventRecord(E->d2h_begin[l], E->s_d2h);
             if (e == cudaSuccess && w_slot) {
                 e = cudaMemcpyAsync(U.w + c.off, s.w + c.off, (size_t)c.len * 2, cudaMemcpyDeviceToHost, E->s_d2h);
                 if (e == cudaSuccess)
-                    e = cudaEventRecord(s.freed[kW][k], E->s_d2h);
+                    e = cudaEventRecord(s.freed[kW][q], E->s_d2h);
             }
             for (int r = 0; r < 3 && e == cudaSuccess; ++r) {
                 e = cudaMemcpyAsync(dst[r] + c.off, s.arr[r] + c.off, (size_t)c.len * 4, cudaMemcpyDeviceToHost,
                                     E->s_d2h);
                 if (e == cudaSuccess)
-                    e = cudaEventRecord(s.freed[r][k], E->s_d2h);
+                    e = cudaEventRecord(s.freed[r][q], E->s_d2h);
             }
         }
         if (e == cudaSuccess && K == 0) {
@@ -440,6 +498,7 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
             e = cudaEventRecord(E->d2h_end[l], E->s_d2h);
         if (e == cudaSuccess) {
             E->recorded[l] = 1;
+            E->host_unit_enqueued[l] = host_ms();
             ++done_units;
         }
     }
@@ -488,21 +547,25 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
 
 // Timeline of the last step: per unit, milliseconds from the step's start to
 // [copy-in begin, master landed, copy-in end, last chunk updated, write-back
-// of the first chunk may begin, write-back end]; then the end of the forward
-// sweep.  NaN where a unit did not get that far.
+// of the first chunk may begin, write-back end] (device events), then [copy-in
+// fully enqueued, update and write-back fully enqueued] (host clock); then the
+// end of the forward sweep.  NaN where a unit did not get that far.
 slide_status engine_timeline(slide_state *st, double *out, int64_t cap)
 {
     StreamEngine *E = st->engine;
     const int L = (int)st->layers.size();
-    if (cap < 6 * (int64_t)L + 1)
-        return fail(SLIDE_ERR_INVALID_ARG, "timeline buffer needs 6 * n_layers + 1 doubles");
+    constexpr int kPer = 8;
+    if (cap < kPer * (int64_t)L + 1)
+        return fail(SLIDE_ERR_INVALID_ARG, "timeline buffer needs 8 * n_layers + 1 doubles");
     const double nan = __builtin_nan("");
     auto since = [&](cudaEvent_t ev) -> double {
         float ms = 0.0f;
         return cudaEventElapsedTime(&ms, E->step_start, ev) == cudaSuccess ? (double)ms : nan;
     };
     for (int l = 0; l < L; ++l) {
-        double *o = out + 6 * l;
+        double *o = out + kPer * l;
+        o[6] = E->host_copyin_enqueued[l];
+        o[7] = E->host_unit_enqueued[l];
         if (!E->recorded[l]) {
             for (int k = 0; k < 6; ++k)
                 o[k] = nan;
@@ -515,7 +578,7 @@ slide_status engine_timeline(slide_state *st, double *out, int64_t cap)
         o[4] = since(E->d2h_begin[l]);
         o[5] = since(E->d2h_end[l]);
     }
-    out[6 * L] = since(E->fwd_done);
+    out[kPer * L] = since(E->fwd_done);
     cudaGetLastError();
     return SLIDE_OK;
 }

@@ -30,7 +30,8 @@ def host_replica_mean(reps_bf16):
     return acc
 
 
-def measure_cpu_reduce_route(S, torch, synth, n, R, seed=1, hp=None, scale=1e-3, return_states=False):
+def measure_cpu_reduce_route(S, torch, synth, n, R, seed=1, hp=None, scale=1e-3, return_states=False,
+                             host_alloc=None):
     """Run one optimizer step of an n-parameter layer by both routes from the
     same master (seeded, m = v = 0, t = 1) on the same R seeded BF16 replicas
     (synth.dev_grad with spec(seed), unit 0, step 1, replica r, `scale`).
@@ -38,7 +39,8 @@ def measure_cpu_reduce_route(S, torch, synth, n, R, seed=1, hp=None, scale=1e-3,
     Returns timings, the host-link bytes each route moved (counted from the
     buffers actually copied) and whether the two final states are
     bit-identical; with return_states=True also both final states as host
-    arrays (master, m, v, BF16 copy)."""
+    arrays (master, m, v, BF16 copy).  host_alloc(shape, dtype) supplies the
+    pinned host buffers (default: torch's pinned allocator)."""
     hp = hp or S.hparams(max_grad_norm=1.0)
     sp = synth.spec(seed)
     reps = [torch.empty(n + 64, dtype=torch.int16, device="cuda") for _ in range(R)]
@@ -47,8 +49,9 @@ def measure_cpu_reduce_route(S, torch, synth, n, R, seed=1, hp=None, scale=1e-3,
     th0 = synth.master(n, seed)
     gpu = S.slide_state_create([n], R)
     cpu = S.slide_state_create([n], 1, flags=S.SLIDE_FLAG_FP32_GRADS)
-    host_reps = [torch.empty(n, dtype=torch.int16, pin_memory=True) for _ in range(R)]
-    mean_host = torch.empty(n, dtype=torch.float32, pin_memory=True)
+    alloc = host_alloc or (lambda shape, dtype: torch.empty(shape, dtype=dtype, pin_memory=True))
+    host_reps = [alloc(n, torch.int16) for _ in range(R)]
+    mean_host = alloc(n, torch.float32)
     mean_dev = torch.empty(n + 64, dtype=torch.float32, device="cuda")
     try:
         S.slide_layer_set(gpu, 0, master=th0, step=0)

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(S):
     lib = C.CDLL(S.LIB_PATH)
     for n in names:
         assert hasattr(lib, n), f"{n} declared in include/ but not exported"
-    assert S.slide_abi_version() == 1
+    assert S.slide_abi_version() == 2
 
 
 def test_every_entry_point_cites_its_passage():
@@ -132,8 +132,15 @@ def test_accounting_streamed_bf16_copy_in_hbm(S):
     (dict(layer_numel=[10], n_replicas=1, residency=7), "residency"),
     (dict(layer_numel=[10], n_replicas=1, chunk_bytes=100), "chunk_bytes"),
     (dict(layer_numel=[10], n_replicas=1, window_layers=3), "window_layers"),
-    (dict(layer_numel=[10], n_replicas=1, flags=16), "flag"),
+    (dict(layer_numel=[10], n_replicas=1, flags=32), "flag"),
     (dict(layer_numel=[], n_replicas=1), "n_layers"),
+    (dict(layer_numel=[10], n_replicas=1, chunk_bytes_d2h=100), "chunk_bytes_d2h"),
+    (dict(layer_numel=[10], n_replicas=1, host_arena=1 << 20, host_arena_bytes=1 << 20), "streamed residency"),
+    (dict(layer_numel=[10], n_replicas=1, residency=1, host_arena=(1 << 20) + 16, host_arena_bytes=1 << 20),
+     "256-byte"),
+    (dict(layer_numel=[10], n_replicas=1, residency=1, host_arena_bytes=1 << 20), "without a host_arena"),
+    (dict(layer_numel=[10], n_replicas=1, residency=1, flags=16, host_arena=1 << 20, host_arena_bytes=1 << 20),
+     "exclude"),
 ])
 def test_config_validation_without_gpu(S, kw, msg):
     numel = kw.pop("layer_numel")

@@ -76,9 +76,14 @@ def test_unit_spread_and_overlap():
         t += dur
     sp = bench.unit_spread(units)
     assert sp["slowest_unit"] == 3
-    assert sp["median_unit_copy_in_ms"] == 20.0
-    assert sp["unit_max_over_median"] == 3.0
-    assert bench.unit_spread(units[:2])["slowest_unit"] is None
+    assert sp["median_unit_copy_in_ms_per_gparam"] == 22.5e9
+    assert sp["unit_max_over_median"] == 60.0 / 22.5
+    # per parameter: unit 0 with twice the parameters is not slow
+    sp = bench.unit_spread(units, sizes=[2, 1, 1, 1, 1, 1])
+    assert sp["slowest_unit"] == 3 and sp["unit_max_over_median"] == 3.0
+    assert bench.unit_spread(units[:1])["slowest_unit"] is None
+    # the last unit of the sweep counts too
+    assert bench.unit_spread(units[:3] + [dict(units[4], h2d_end=units[4]["h2d_begin"] + 200.0)])["slowest_unit"] == 3
     units[2] = {k: nan for k in units[2]}
     assert bench.unit_spread(units)["slowest_unit"] == 3
     ov = bench.timeline_overlap([u for u in units if u["h2d_begin"] == u["h2d_begin"]], 10.0)
@@ -164,9 +169,10 @@ def _full_record():
                              "gpu_route": {"s": 0.002, "link_bytes": 0},
                              "cpu_route": {"s": 3.0, "d2h_bytes": 2 * R * n, "h2d_bytes": 4 * n,
                                            "link_bytes": 2 * R * n + 4 * n}},
-        "chunk_sweep": {"workload": "h8192x8_streamed", "chosen": [64, 64],
-                        "points": [{"h2d_mib": a, "d2h_mib": b, "frac": 0.9, "s_per_step": 0.7}
-                                   for a in (16, 32, 64, 128) for b in (16, 64, 256)]},
+        "chunk_sweep": {k: {"workload": k, "chosen": [64, 64],
+                            "points": [{"h2d_mib": a, "d2h_mib": b, "frac": 0.9, "s_per_step": 0.7}
+                                       for a in (32, 64, 128, 256) for b in (64, 256)]}
+                        for k in ("h8192x8_streamed", "h5120x40_streamed")},
         "streamed": streamed,
         "streamed_also": {"h5120x40_streamed": dict(streamed, workload="h5120x40_streamed",
                                                     bf16_copy_in_hbm=True),
@@ -201,5 +207,30 @@ def test_compact_headline_is_last_and_small(capsys, tmp_path):
     assert st["h8192x8_streamed"]["frac"] == 0.97 and st["h8192x8_streamed"]["unit_max_over_median"] == 1.1
     assert "skipped" in st["h8192x8_streamed+x"]
     assert st["h5120x40_streamed"]["bf16_in_hbm"] is True
-    assert len(h["chunk_sweep"]["points"]) == 12
+    assert len(h["chunk_sweep"]["h5120x40_streamed"]["points"]) == 8
     assert json.load(open(out))["streamed"]["timeline_fastest_step"]["units_ms"][0]["h2d_begin"] == 0.0
+
+
+def test_pinned_arena_carving():
+    """The run's arena hands out 256-byte aligned, non-overlapping pieces,
+    and a reset makes its space reusable by the next leg."""
+    import numpy as np
+    import torch
+    backing = np.zeros(1 << 20, np.uint8)
+    a = object.__new__(bench.PinnedArena)
+    a.addr, a.nbytes, a.top = (backing.ctypes.data + 255) // 256 * 256, (1 << 20) - 256, 0
+    t1 = a.tensor(1000, torch.int16)
+    t2 = a.tensor((3, 5), torch.float32)
+    assert t1.data_ptr() % 256 == 0 and t2.data_ptr() % 256 == 0
+    assert t2.data_ptr() >= t1.data_ptr() + 2000
+    t1.fill_(7)
+    t2.fill_(1.5)
+    assert int(t1.sum()) == 7000 and float(t2.sum()) == 22.5
+    m = a.mark()
+    p = a.carve(4096)
+    a.reset(m)
+    assert a.carve(4096) == p
+    with pytest.raises(MemoryError):
+        a.carve(1 << 21)
+    a.reset()
+    assert a.tensor(10, torch.uint8).data_ptr() == a.addr

@@ -79,6 +79,12 @@ def check_timeline(S, st, sizes):
         assert u["update_end"] <= u["d2h_end"] + eps and u["d2h_begin"] <= u["d2h_end"] + eps, u
     ends = [u["d2h_end"] for u in units]
     assert all(ends[l] >= ends[l + 1] - eps for l in range(len(units) - 1))
+    # host enqueue order: a unit's copy-in is enqueued before its update, and
+    # the units of the reverse sweep one after another
+    for l, u in enumerate(units):
+        assert u["host_copyin_enqueued"] <= u["host_unit_enqueued"], u
+        if l + 1 < len(units):
+            assert units[l + 1]["host_unit_enqueued"] <= u["host_unit_enqueued"], (l, u)
 
 
 def toy(R=3, clip=0.0, seed=5, fp32=False):
@@ -87,16 +93,38 @@ def toy(R=3, clip=0.0, seed=5, fp32=False):
                       R=R, steps=3, seed=seed, max_grad_norm=clip, lr=1e-3, streamed=True, fp32_grads=fp32)
 
 
-@pytest.mark.parametrize("clip,chunk,fp32,in_hbm", [(0.0, 64 << 10, False, False), (0.5, 256, False, False),
-                                                    (1e4, 1 << 20, False, False), (0.0, 64 << 10, True, False),
-                                                    (0.5, 4096, True, False), (0.0, 64 << 10, False, True),
-                                                    (0.5, 4096, True, True)])
-def test_streamed_toy_every_element(S, clip, chunk, fp32, in_hbm):
+def pinned_arena(nbytes):
+    """Caller-owned pinned host memory of at least nbytes, 256-byte aligned:
+    (keep-alive tensor, address)."""
+    t = torch.empty(nbytes + 256, dtype=torch.uint8, pin_memory=True)
+    addr = (t.data_ptr() + 255) // 256 * 256
+    return t, addr
+
+
+@pytest.mark.parametrize("clip,chunk,chunk_d2h,fp32,in_hbm,arena", [
+    (0.0, 64 << 10, 0, False, False, False), (0.5, 256, 0, False, False, False),
+    (1e4, 1 << 20, 0, False, False, False), (0.0, 64 << 10, 0, True, False, False),
+    (0.5, 4096, 0, True, False, False), (0.0, 64 << 10, 0, False, True, False),
+    (0.5, 4096, 0, True, True, False),
+    # write-back chunks smaller, larger and not a multiple of the copy-in chunks
+    (0.0, 64 << 10, 4096, False, False, False), (0.5, 4096, 64 << 10, False, False, True),
+    (0.0, 1024, 3072, True, True, True), (0.0, 768, 1 << 20, False, True, False),
+    (1e-3, 3072, 1024, False, False, True)])
+def test_streamed_toy_every_element(S, clip, chunk, chunk_d2h, fp32, in_hbm, arena):
     w = toy(clip=clip, fp32=fp32)
     flags = (S.SLIDE_FLAG_FP32_GRADS if fp32 else 0) | (S.SLIDE_FLAG_BF16_COPY_IN_HBM if in_hbm else 0)
-    st = S.slide_state_create([u.numel for u in w.units], w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED,
-                              chunk_bytes=chunk, flags=flags)
+    sizes = [u.numel for u in w.units]
+    keep, addr, nbytes = None, None, 0
+    if arena:
+        nbytes = S.slide_state_bytes(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED, flags=flags)[1]
+        keep, addr = pinned_arena(nbytes)
+        keep.fill_(0x5A)          # the state must zero what it uses
+    st = S.slide_state_create(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED,
+                              chunk_bytes=chunk, chunk_bytes_d2h=chunk_d2h, flags=flags,
+                              host_arena=addr, host_arena_bytes=nbytes)
     try:
+        if arena:
+            assert S.slide_layer_ptrs(st, 0)[0] == addr
         init_streamed(S, w, st)
         ref = []
         for ui, u in enumerate(w.units):
@@ -123,6 +151,66 @@ def test_streamed_toy_every_element(S, clip, chunk, fp32, in_hbm):
             check_timeline(S, st, [u.numel for u in w.units])
     finally:
         S.slide_state_destroy(st)
+
+
+def test_streamed_caller_arena_reused_by_states(S):
+    """One caller-owned pinned arena serves two states in turn: the first
+    state's steps leave it dirty, the second starts from zero state (the
+    state zeroes what it uses), steps against the oracle, and destroying a
+    state leaves the arena to its owner."""
+    w1 = toy(R=2, seed=8)
+    w2 = W.Workload("toy2", [W.Unit("a", [("a", 300_001)]), W.Unit("b", [("b", 65_537)])], R=4, steps=2, seed=9,
+                    lr=1e-3, streamed=True)
+    need = max(S.slide_state_bytes([u.numel for u in w.units], w.R,
+                                   residency=S.SLIDE_RESIDENCY_HOST_STREAMED)[1] for w in (w1, w2))
+    keep, addr = pinned_arena(need)
+    for w in (w1, w2):
+        sizes = [u.numel for u in w.units]
+        st = S.slide_state_create(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED, chunk_bytes=8192,
+                                  host_arena=addr, host_arena_bytes=need)
+        try:
+            for ui, u in enumerate(w.units):
+                m = np.empty(u.numel, np.float32)
+                S.slide_layer_get(st, ui, m=m)
+                assert not m.any()
+            init_streamed(S, w, st)
+            ref = [[synth.master(u.numel, w.seed, unit=ui), np.zeros(u.numel, np.float32),
+                    np.zeros(u.numel, np.float32), np.zeros(u.numel, np.uint16)] for ui, u in enumerate(w.units)]
+            hp = S.hparams(*w.hparams_tuple())
+            for t in range(1, w.steps + 1):
+                holder = ModelGradsHolder(w, t)
+                S.slide_model_step_streamed(st, synth.grad_fn_address(), holder.mg, hp)
+                for ui, u in enumerate(w.units):
+                    oracle.layer_step([pu.unit_grad_host(w, ui, t, r) for r in range(w.R)], *ref[ui],
+                                      pu.hp_oracle(w), t)
+            for ui, u in enumerate(w.units):
+                a, b, c = (np.empty(u.numel, np.float32) for _ in range(3))
+                wb = np.empty(u.numel, np.uint16)
+                S.slide_layer_get(st, ui, a, b, c, wb)
+                rep = [pu.compare_fp32("theta", a, ref[ui][0]), pu.compare_fp32("m", b, ref[ui][1]),
+                       pu.compare_fp32("v", c, ref[ui][2]), pu.compare_bf16("w", wb, ref[ui][3])]
+                pu.assert_parity(rep)
+                assert all(r["not_bit_equal"] == 0 for r in rep), rep
+        finally:
+            S.slide_state_destroy(st)
+    keep.fill_(1)                       # still the caller's memory
+    assert int(keep[addr - keep.data_ptr()]) == 1
+
+
+def test_streamed_caller_arena_rejected(S):
+    sizes = [10_000]
+    need = S.slide_state_bytes(sizes, 1, residency=S.SLIDE_RESIDENCY_HOST_STREAMED)[1]
+    keep, addr = pinned_arena(need)
+    with pytest.raises(S.SlideError) as e:
+        S.slide_state_create(sizes, 1, residency=S.SLIDE_RESIDENCY_HOST_STREAMED, host_arena=addr,
+                             host_arena_bytes=need - 256)
+    assert e.value.status == S.SLIDE_ERR_INVALID_ARG and "smaller" in str(e.value)
+    pageable = np.zeros(need + 256, np.uint8)
+    paddr = (pageable.ctypes.data + 255) // 256 * 256
+    with pytest.raises(S.SlideError) as e:
+        S.slide_state_create(sizes, 1, residency=S.SLIDE_RESIDENCY_HOST_STREAMED, host_arena=paddr,
+                             host_arena_bytes=need)
+    assert e.value.status == S.SLIDE_ERR_INVALID_ARG and "pinned" in str(e.value)
 
 
 def test_streamed_python_callback_sees_master_and_errors_abort(S):
