@@ -73,8 +73,9 @@ def parse_args():
     ap.add_argument("--streamed-arena", choices=["hostalloc", "hugepages"], default="hostalloc",
                     help="pinned host arena of the streamed legs: cudaHostAlloc, or an anonymous mapping "
                          "advised for transparent huge pages and registered with cudaHostRegister")
-    ap.add_argument("--streamed-chunk-mib", type=int, default=64,
-                    help="host->device copy chunk of the streamed engine (the pages' 64 MiB by default)")
+    ap.add_argument("--streamed-chunk-mib", type=int, default=256,
+                    help="host->device copy chunk of the streamed engine (the library's default, 256 MiB, "
+                         "from the chunk sweep; the pages use 64 MiB)")
     ap.add_argument("--streamed-chunk-d2h-mib", type=int, default=0,
                     help="device->host write-back chunk of the streamed engine (0: as the copy-in chunk)")
     ap.add_argument("--chunk-sweep", default="32:32,64:64,128:128,256:256,512:512,64:256,256:64,128:512",
@@ -364,6 +365,24 @@ def mem_available_bytes():
     except OSError:
         pass
     return 0
+
+
+def hbm_read_probe(torch, nbytes=4 << 30, reps=10):
+    """Read-only HBM bandwidth for context (the clip pre-pass is a read-only
+    stream; the roofline peak is a copy): torch's sum over nbytes of int32,
+    CUDA events, median of reps.  A library kernel, reported beside the
+    pre-pass, never used as a denominator."""
+    x = torch.ones(nbytes // 4, dtype=torch.int32, device="cuda")
+    out = []
+    for _ in range(reps + 2):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        x.sum()
+        b.record()
+        torch.cuda.synchronize()
+        out.append(nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
+    del x
+    return {"gbs": statistics.median(out[2:]), "how": f"torch int32 sum over {nbytes >> 30} GiB, median of {reps}"}
 
 
 def release_pinned_cache(torch):
@@ -1027,6 +1046,7 @@ def run_ours(args):
     del batches
     release_pinned_cache(torch)
     torch.cuda.empty_cache()
+    read_probe = hbm_read_probe(torch) if world == 1 else None
     variant = None
     cpu_route = None
     others = None
@@ -1120,8 +1140,9 @@ def run_ours(args):
                      "traffic": traffic, "traffic_note": traffic_note, "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                      "bytes_per_launch": bytes_upd, "avg_launch_ms": upd_avg,
                      "bytes_per_param": 26 + 2 * R, "launches": K},
-        "prepass": ({"kernel": "grad_sqnorm", "achieved": ach_pre, "unit": "GB/s", "frac": ach_pre / peak,
+        "prepass": ({"kernel": "grad_sqnorm_pipe", "achieved": ach_pre, "unit": "GB/s", "frac": ach_pre / peak,
                      "bytes_per_launch": bytes_pre, "avg_launch_ms": pre_avg} if clip else None),
+        "hbm_read_probe": read_probe,
         "step_roofline_frac": (step_bytes / (ms_step * 1e-3) / 1e9) / peak,
         "gpu_launches": K * (2 if clip else 1),
         "clocks": clocks,
@@ -1218,6 +1239,8 @@ def compact_headline(full):
     if full.get("prepass"):
         line["prepass"] = _pick(full["prepass"], ("kernel", "achieved", "frac", "avg_launch_ms"))
     line["gpu_launches"] = full["gpu_launches"]
+    if full.get("hbm_read_probe"):
+        line["hbm_read_probe_gbs"] = _r(full["hbm_read_probe"]["gbs"])
     ck = full.get("clocks") or {}
     line["clocks"] = {"sm_mhz": ck.get("sm_mhz"), "sm_max_mhz": ck.get("sm_max_mhz"),
                       "reasons": ck.get("reasons", []), "samples": ck.get("samples")}

@@ -129,7 +129,7 @@ typedef struct {
     uint32_t timeout_ms;         /* streamed: bound of each host wait (0 = 600000) */
     uint32_t flags;              /* SLIDE_FLAG_* */
     int64_t chunk_bytes;         /* streamed: host->device chunk of master, m and v, and the
-                                    update's chunk (0 = 64 MiB); bytes of FP32, multiple of 256 */
+                                    update's chunk (0 = 256 MiB); bytes of FP32, multiple of 256 */
     int64_t chunk_bytes_d2h;     /* streamed: device->host write-back chunk (0 = chunk_bytes);
                                     bytes of FP32, multiple of 256 */
     void *host_arena;            /* streamed: caller-owned pinned host memory (cudaHostAlloc, or

@@ -33,11 +33,11 @@
 // power of two).
 //
 // The optional global clip needs the norm of the whole layer's mean gradient
-// before any element is updated, so it is a separate pre-pass (k_grad_sqnorm)
-// that re-reads the replicas (2R bytes per parameter) and writes one
-// double-precision partial per block; the fused kernel turns the partials
-// into the coefficient in its prologue, in the same fixed order in every
-// block, so every block uses the same bits.
+// before any element is updated, so it is a separate pre-pass
+// (k_grad_sqnorm_pipe, the same bulk-copy pipeline reading only the replicas:
+// 2R bytes per parameter) that writes one double-precision partial per block;
+// the fused kernel turns the partials into the coefficient in its prologue,
+// in the same fixed order in every block, so every block uses the same bits.
 //
 // Every wait on an mbarrier is bounded (kWaitLimitNs of wall time); a wait
 // that runs out sets bit 1 of the status word, waits (bounded) for the bulk
@@ -53,7 +53,7 @@
 namespace slide {
 namespace {
 
-constexpr int kThreads = 256;            // register-path kernels
+constexpr int kThreads = 256;            // block size of the small helper kernels
 constexpr int kTile = 2048;              // parameters per pipeline tile
 constexpr int kStages = 2;               // shared-memory ring depth
 constexpr int kConsumerWarps = 8;        // kTile = 256 consumer threads x 8 parameters
@@ -353,11 +353,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_grad_reduce_adamw_cast(KArg
             return;
         int stage = 0;
         uint32_t phase = 0;
-        int issued[kStages];
-        uint32_t issued_phase[kStages];
-#pragma unroll
-        for (int i = 0; i < kStages; ++i)
-            issued[i] = 0, issued_phase[i] = 0;
+        uint32_t issued = 0, issued_phase = 0;  // per stage: filled at least once, and that fill's parity
         bool ok = true;
         for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
             if (!mbar_wait(&empty[stage], phase ^ 1u)) {
@@ -374,8 +370,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_grad_reduce_adamw_cast(KArg
             bulk_load(base + R * P::kGradBytes, a.theta + e0, P::kF32Bytes, &full[stage]);
             bulk_load(base + R * P::kGradBytes + P::kF32Bytes, a.m + e0, P::kF32Bytes, &full[stage]);
             bulk_load(base + R * P::kGradBytes + 2 * P::kF32Bytes, a.v + e0, P::kF32Bytes, &full[stage]);
-            issued[stage] = 1;
-            issued_phase[stage] = phase;
+            issued |= 1u << stage;
+            issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
             if (++stage == kStages) {
                 stage = 0;
                 phase ^= 1u;
@@ -384,7 +380,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_grad_reduce_adamw_cast(KArg
         // No copy may still be landing in shared memory when the block ends:
         // wait (bounded) for the last fill of every stage.
         for (int i = 0; i < kStages; ++i)
-            if (issued[i] && !mbar_wait(&full[i], issued_phase[i]))
+            if (((issued >> i) & 1u) && !mbar_wait(&full[i], (issued_phase >> i) & 1u))
                 ok = false;
         if (!ok && a.status)
             atomicOr(a.status, kStatusWaitLimit);
@@ -505,64 +501,176 @@ struct SqArgs {
     ReplicaPtrs g;
     int64_t n;
     double *partials;
+    unsigned *status;  // bit 1: a bounded wait ran out (may be NULL)
 };
 
-template <typename G, int R, int UNROLL>
-__global__ void __launch_bounds__(kThreads) k_grad_sqnorm(SqArgs a)
+// Clip pre-pass as a bulk-copy pipeline, the fused kernel's structure for a
+// read-only pass: one CTA per SM; a producer lane streams tiles of 4 KiB per
+// replica (2048 BF16 or 1024 FP32 parameters) into a ring of up to 8 stages
+// (at most 192 KiB), and 8 consumer warps read them from shared memory and
+// accumulate the squared replica means.  The loads in flight sit in shared
+// memory, not in registers.  Tile and ring sizes were chosen by timing the
+// whole clipped step: 4 KiB tiles in 8 stages beat 8 KiB tiles, 4, 6 or 12
+// stages, and the register-path kernel this replaced.  The part after the
+// last whole tile is read with plain vector loads by one CTA.  Each block
+// writes one double partial, in a fixed order.
+template <typename G, int R>
+struct SqPipe {
+    static constexpr uint32_t kGradBytes = 4096;                 // per replica per tile
+    static constexpr int kTile = (int)(kGradBytes / sizeof(G));  // parameters per tile
+    static constexpr int kPer = (int)(16 / sizeof(G));           // parameters per 16-byte vector
+    static constexpr uint32_t kStageBytes = R * kGradBytes;
+    static constexpr int kFit = (int)((192u * 1024u) / kStageBytes);
+    static constexpr int kStages = kFit > 8 ? 8 : (kFit < 2 ? 2 : kFit);
+    static constexpr uint32_t kSmemBytes = kStages * kStageBytes + 2 * kStages * 8;
+    static constexpr int kVec = (int)(kGradBytes / (16 * kConsumerWarps * 32));  // vectors per thread per replica
+    static_assert(kVec >= 1 && kGradBytes == (uint32_t)kVec * 16 * kConsumerWarps * 32,
+                  "a tile is a whole number of 16-byte vectors per consumer thread");
+};
+
+// Element e of a 16-byte vector of gradient values, widened to FP32.
+template <typename G>
+__device__ __forceinline__ float vec16_at(const uint4 &q, int e)
 {
-    const int64_t nvec = a.n >> 3;
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
-    const int64_t tid = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-    SqAcc acc;
-    for (int64_t k0 = tid; k0 < nvec; k0 += stride * UNROLL) {
-        typename GradT<G>::Raw8 raw[UNROLL][R];
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
-            const int64_t k = k0 + (int64_t)u * stride;
-            if (k < nvec) {
-#pragma unroll
-                for (int r = 0; r < R; ++r)
-                    raw[u][r] = GradT<G>::load8(a.g.p[r], k);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
-            const int64_t k = k0 + (int64_t)u * stride;
-            if (k < nvec) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    float x[R];
-#pragma unroll
-                    for (int r = 0; r < R; ++r)
-                        x[r] = GradT<G>::at8(raw[u][r], e);
-                    acc.add(replica_mean<R>(x));
-                }
-            }
-        }
+    if constexpr (sizeof(G) == 2) {
+        const uint32_t word = (&q.x)[e >> 1];
+        return (e & 1) ? bf16_hi(word) : bf16_lo(word);
+    } else {
+        return __uint_as_float((&q.x)[e]);
     }
-    const int64_t tail0 = nvec << 3;
-    if (tid < a.n - tail0) {
-        const int64_t i = tail0 + tid;
+}
+
+template <typename G, int R>
+__device__ __forceinline__ void sq_add_vec16(SqAcc &acc, const uint4 (&q)[R])
+{
+#pragma unroll
+    for (int e = 0; e < SqPipe<G, R>::kPer; ++e) {
         float x[R];
 #pragma unroll
         for (int r = 0; r < R; ++r)
-            x[r] = GradT<G>::one(static_cast<const G *>(a.g.p[r]), i);
+            x[r] = vec16_at<G>(q[r], e);
         acc.add(replica_mean<R>(x));
     }
+}
 
-    // Block reduction in double, fixed order: shuffle-down tree per warp,
-    // then warp 0 over the warps' results.
+template <typename G, int R>
+__global__ void __launch_bounds__(kPipeThreads, 1) k_grad_sqnorm_pipe(SqArgs a)
+{
+    using P = SqPipe<G, R>;
+    extern __shared__ __align__(128) unsigned char smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + P::kStages * P::kStageBytes);
+    uint64_t *empty = full + P::kStages;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < P::kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], kConsumerWarps);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    const int64_t ntiles = a.n / P::kTile;
+    SqAcc acc;
+
+    if (warp == kConsumerWarps) {
+        // ---- producer: lane 0 issues the bulk copies; the warp then joins the reduction ----
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t issued = 0, issued_phase = 0;  // per stage: filled at least once, and that fill's parity
+            bool ok = true;
+            for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+                if (!mbar_wait(&empty[stage], phase ^ 1u)) {
+                    ok = false;
+                    break;
+                }
+                unsigned char *base = smem + stage * P::kStageBytes;
+                mbar_arrive_expect_tx(&full[stage], P::kStageBytes);
+                const int64_t e0 = tile * P::kTile;
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    bulk_load(base + r * P::kGradBytes, static_cast<const G *>(a.g.p[r]) + e0, P::kGradBytes,
+                              &full[stage]);
+                issued |= 1u << stage;
+                issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                if (++stage == P::kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            // no copy may still be landing in shared memory when the block ends
+            for (int i = 0; i < P::kStages; ++i)
+                if (((issued >> i) & 1u) && !mbar_wait(&full[i], (issued_phase >> i) & 1u))
+                    ok = false;
+            if (!ok && a.status)
+                atomicOr(a.status, kStatusWaitLimit);
+        }
+        __syncwarp();
+    } else {
+        // ---- consumers: thread c reads vectors c, c + 256, ... of every replica of a tile ----
+        const int c = threadIdx.x;
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+            const bool landed = __all_sync(0xffffffffu, mbar_wait(&full[stage], phase));
+            if (!landed) {  // the whole warp gives up together
+                if (lane == 0 && a.status)
+                    atomicOr(a.status, kStatusWaitLimit);
+                break;
+            }
+            const unsigned char *base = smem + stage * P::kStageBytes;
+            uint4 q[P::kVec][R];
+#pragma unroll
+            for (int j = 0; j < P::kVec; ++j)
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    q[j][r] = *reinterpret_cast<const uint4 *>(base + r * P::kGradBytes + j * 4096 + c * 16);
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(&empty[stage]);
+#pragma unroll
+            for (int j = 0; j < P::kVec; ++j)
+                sq_add_vec16<G, R>(acc, q[j]);
+            if (++stage == P::kStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        // the part after the last whole tile, by one CTA, plain loads
+        if (blockIdx.x == (unsigned)(ntiles % gridDim.x)) {
+            const int64_t base_e = ntiles * P::kTile;
+            const int64_t rem = a.n - base_e;  // < kTile
+            const int64_t nvec = rem / P::kPer;
+            for (int64_t q = c; q < nvec; q += kConsumerWarps * 32) {
+                uint4 v[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    v[r] = __ldcs(reinterpret_cast<const uint4 *>(static_cast<const G *>(a.g.p[r]) + base_e) + q);
+                sq_add_vec16<G, R>(acc, v);
+            }
+            const int64_t tail0 = base_e + nvec * P::kPer;
+            if (c < a.n - tail0) {
+                const int64_t i = tail0 + c;
+                float x[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    x[r] = GradT<G>::one(static_cast<const G *>(a.g.p[r]), i);
+                acc.add(replica_mean<R>(x));
+            }
+        }
+    }
+
+    // Block reduction in double, fixed order (the producer warp adds zeros).
     double d = (double)acc.hi + (double)acc.lo + (double)acc.err;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1)
         d += __shfl_down_sync(0xffffffffu, d, off);
-    __shared__ double s_warp[kThreads / 32];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    __shared__ double s_warp[kConsumerWarps + 1];
     if (lane == 0)
         s_warp[warp] = d;
     __syncthreads();
     if (warp == 0) {
-        d = lane < kThreads / 32 ? s_warp[lane] : 0.0;
+        d = lane < kConsumerWarps + 1 ? s_warp[lane] : 0.0;
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1)
             d += __shfl_down_sync(0xffffffffu, d, off);
@@ -590,39 +698,7 @@ int sm_count(int device)
     return c;
 }
 
-// Resident blocks per SM of a register-path kernel, cached per (kernel, device).
-template <auto Kernel>
-int blocks_per_sm(int device)
-{
-    static std::atomic<int> cache[kMaxDevices];
-    if (device < 0 || device >= kMaxDevices)
-        return 1;
-    int b = cache[device].load(std::memory_order_relaxed);
-    if (b == 0) {
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, Kernel, kThreads, 0) != cudaSuccess || b < 1)
-            b = 1;
-        cache[device].store(b, std::memory_order_relaxed);
-    }
-    return b;
-}
 
-// Persistent grid for a register-path kernel: SMs x resident blocks, fewer
-// if there is less work.
-template <auto Kernel>
-unsigned grid_for(int device, int64_t n, int cap)
-{
-    const int64_t work = ((n >> 3) + kThreads - 1) / kThreads;  // blocks of 8-wide vectors
-    int64_t g = (int64_t)sm_count(device) * blocks_per_sm<Kernel>(device);
-    if (g > work)
-        g = work;
-    if (g > cap)
-        g = cap;
-    if (g < 1)
-        g = 1;
-    return (unsigned)g;
-}
-
-constexpr int kUnrollSq = 2;
 
 // Raise the fused kernel's dynamic shared-memory limit on `device` (once per
 // device; the device must be current).  Setting the attribute also loads the
@@ -687,15 +763,43 @@ cudaError_t launch_step_g(const KArgs &a, int R, bool clip, bool check, int devi
     }
 }
 
+// Raise the pipelined pre-pass's dynamic shared-memory limit on `device`
+// (once per device; the device must be current; also loads its code).
+template <typename G, int R>
+cudaError_t prepare_sq_pipe(int device)
+{
+    static std::atomic<int> attr_set[kMaxDevices];
+    if (device >= 0 && device < kMaxDevices && attr_set[device].load(std::memory_order_acquire))
+        return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(k_grad_sqnorm_pipe<G, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SqPipe<G, R>::kSmemBytes);
+    if (e != cudaSuccess)
+        return e;
+    if (device >= 0 && device < kMaxDevices)
+        attr_set[device].store(1, std::memory_order_release);
+    return cudaSuccess;
+}
+
 template <typename G, int R>
 cudaError_t launch_sq_r(const SqArgs &a, int *n_partials, int device, cudaStream_t stream)
 {
-    constexpr auto kern = k_grad_sqnorm<G, R, kUnrollSq>;
-    unsigned grid = grid_for<kern>(device, a.n, kMaxPartials);
-    kern<<<grid, kThreads, 0, stream>>>(a);
+    using P = SqPipe<G, R>;
+    static_assert(P::kSmemBytes <= 227 * 1024, "pre-pass stages exceed the shared memory of a CTA");
+    cudaError_t e = prepare_sq_pipe<G, R>(device);
+    if (e != cudaSuccess)
+        return e;
+    // one CTA per SM, never more CTAs than whole tiles (at least one, for the tail)
+    int64_t grid = sm_count(device);
+    const int64_t ntiles = a.n / P::kTile;
+    if (grid > ntiles)
+        grid = ntiles > 0 ? ntiles : 1;
+    if (grid > kMaxPartials)
+        grid = kMaxPartials;
+    k_grad_sqnorm_pipe<G, R><<<(unsigned)grid, kPipeThreads, P::kSmemBytes, stream>>>(a);
     *n_partials = (int)grid;
     return cudaGetLastError();
 }
+
 
 __global__ void k_cast_bf16(const float *src, uint16_t *w, int64_t n)
 {
@@ -753,7 +857,7 @@ cudaError_t launch_sq_g(const SqArgs &a, int R, int *n_partials, int device, cud
 cudaError_t launch_grad_sqnorm(const ReplicaPtrs &g, int R, int64_t n, const ClipScratch &scratch,
                                int *n_partials, int device, cudaStream_t stream, bool f32_grads)
 {
-    SqArgs a{g, n, scratch.partials};
+    SqArgs a{g, n, scratch.partials, scratch.status};
     return f32_grads ? launch_sq_g<float>(a, R, n_partials, device, stream)
                      : launch_sq_g<uint16_t>(a, R, n_partials, device, stream);
 }
@@ -766,14 +870,11 @@ namespace {
 template <int R>
 cudaError_t preload_bf16_r(int device)
 {
-    cudaFuncAttributes fa;
     cudaError_t e = prepare_pipeline_kernel<uint16_t, R, true, false>(device);
     if (e == cudaSuccess)
         e = prepare_pipeline_kernel<uint16_t, R, false, false>(device);
     if (e == cudaSuccess)
-        e = cudaFuncGetAttributes(&fa, k_grad_sqnorm<uint16_t, R, kUnrollSq>);
-    if (e == cudaSuccess)
-        blocks_per_sm<k_grad_sqnorm<uint16_t, R, kUnrollSq>>(device);
+        e = prepare_sq_pipe<uint16_t, R>(device);
     return e;
 }
 

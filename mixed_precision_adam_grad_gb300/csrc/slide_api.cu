@@ -275,8 +275,8 @@ slide_status slide_state_create(const slide_config *cfg, slide_state **out)
         st->cfg.window_layers = 2;
     if (st->cfg.timeout_ms == 0)
         st->cfg.timeout_ms = 600000;
-    if (st->cfg.chunk_bytes == 0)
-        st->cfg.chunk_bytes = (int64_t)64 << 20;
+    if (st->cfg.chunk_bytes == 0)  // chosen by a sweep of both chunk sizes on the 8 x h8192 and 40 x h5120 models
+        st->cfg.chunk_bytes = (int64_t)256 << 20;
     if (st->cfg.chunk_bytes_d2h == 0)
         st->cfg.chunk_bytes_d2h = st->cfg.chunk_bytes;
     st->device = cfg->device;
