@@ -367,24 +367,6 @@ def mem_available_bytes():
     return 0
 
 
-def hbm_read_probe(torch, nbytes=4 << 30, reps=10):
-    """Read-only HBM bandwidth for context (the clip pre-pass is a read-only
-    stream; the roofline peak is a copy): torch's sum over nbytes of int32,
-    CUDA events, median of reps.  A library kernel, reported beside the
-    pre-pass, never used as a denominator."""
-    x = torch.ones(nbytes // 4, dtype=torch.int32, device="cuda")
-    out = []
-    for _ in range(reps + 2):
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        x.sum()
-        b.record()
-        torch.cuda.synchronize()
-        out.append(nbytes / (a.elapsed_time(b) * 1e-3) / 1e9)
-    del x
-    return {"gbs": statistics.median(out[2:]), "how": f"torch int32 sum over {nbytes >> 30} GiB, median of {reps}"}
-
-
 def release_pinned_cache(torch):
     """Return the pinned host buffers that torch keeps cached after their
     tensors are freed, so the streamed legs can pin the host state."""
@@ -1046,7 +1028,6 @@ def run_ours(args):
     del batches
     release_pinned_cache(torch)
     torch.cuda.empty_cache()
-    read_probe = hbm_read_probe(torch) if world == 1 else None
     variant = None
     cpu_route = None
     others = None
@@ -1142,7 +1123,6 @@ def run_ours(args):
                      "bytes_per_param": 26 + 2 * R, "launches": K},
         "prepass": ({"kernel": "grad_sqnorm_pipe", "achieved": ach_pre, "unit": "GB/s", "frac": ach_pre / peak,
                      "bytes_per_launch": bytes_pre, "avg_launch_ms": pre_avg} if clip else None),
-        "hbm_read_probe": read_probe,
         "step_roofline_frac": (step_bytes / (ms_step * 1e-3) / 1e9) / peak,
         "gpu_launches": K * (2 if clip else 1),
         "clocks": clocks,
@@ -1239,8 +1219,6 @@ def compact_headline(full):
     if full.get("prepass"):
         line["prepass"] = _pick(full["prepass"], ("kernel", "achieved", "frac", "avg_launch_ms"))
     line["gpu_launches"] = full["gpu_launches"]
-    if full.get("hbm_read_probe"):
-        line["hbm_read_probe_gbs"] = _r(full["hbm_read_probe"]["gbs"])
     ck = full.get("clocks") or {}
     line["clocks"] = {"sm_mhz": ck.get("sm_mhz"), "sm_max_mhz": ck.get("sm_max_mhz"),
                       "reasons": ck.get("reasons", []), "samples": ck.get("samples")}
