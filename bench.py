@@ -883,13 +883,17 @@ def run_ours(args):
         also = [x for x in args.streamed_also.split(",") if x and x != args.streamed_workload]
         streamed_keys = [] if args.no_streamed else [args.streamed_workload] + also
         needs = [0 if args.no_e2e else 2 * (2 * R * n + 2 * n) + (1 << 20)]
-        if args.pinned_guard_gib > 0 and (streamed_keys or not args.no_e2e):
-            guard = PinnedArena(args.pinned_guard_gib << 30)
-        avail = mem_available_bytes() - (16 << 30)
-        needs += [b for b in (streamed_host_bytes(S, k, args) + PROBE_BYTES for k in streamed_keys)
-                  if b <= avail]
-        if args.streamed_arena == "hostalloc" and max(needs) > 0:
-            arena = PinnedArena(max(needs))
+        try:
+            if args.pinned_guard_gib > 0 and (streamed_keys or not args.no_e2e):
+                guard = PinnedArena(args.pinned_guard_gib << 30)
+            avail = mem_available_bytes() - (16 << 30)
+            needs += [b for b in (streamed_host_bytes(S, k, args) + PROBE_BYTES for k in streamed_keys)
+                      if b <= avail]
+            if args.streamed_arena == "hostalloc" and max(needs) > 0:
+                arena = PinnedArena(max(needs))
+        except (OSError, MemoryError) as exc:   # no arena: every state pins its own host memory
+            print(f"detail {json.dumps({'pinned_arena_unavailable': str(exc)})}", flush=True)
+            arena = None
 
     st = S.slide_state_create([n], R, device=local)
     try:
