@@ -147,9 +147,12 @@ typedef struct slide_state slide_state; /* opaque; owns all of its memory */
  * fill the R replica buffers replica_dev_ptrs[0..R-1] of unit `layer` (device
  * pointers into the window, each layer_numel[layer] BF16 values, or FP32 values
  * with SLIDE_FLAG_FP32_GRADS; owned by the state) with work enqueued on
- * `stream`.  replica_dev_ptrs[R] points to
- * the unit's FP32 master weights in the window, the version being updated
- * (read-only), as a backward pass would read them.  Return 0 on success; any
+ * `stream`.  replica_dev_ptrs[R] points to the unit's weights as a backward
+ * pass would read them, the version being updated (read-only): the FP32 master
+ * in the window (layer_numel[layer] floats; the callback runs once it has
+ * landed), or, with SLIDE_FLAG_BF16_COPY_IN_HBM, the unit's resident BF16
+ * compute copy (layer_numel[layer] BF16 values; the callback runs at once and
+ * master, m and v arrive chunk by chunk behind it).  Return 0 on success; any
  * other value aborts the sweep. */
 typedef int (*slide_grad_fn)(void *user, int32_t layer, void *const *replica_dev_ptrs,
                              slide_stream_t stream);
@@ -369,7 +372,9 @@ SLIDE_API slide_status slide_deliver_bf16(slide_state *st, int32_t layer, void *
 /* Timeline of the last slide_model_step_streamed, for tracing how the copies
  * and the updates overlap (host-streamed residency).  out receives, for each
  * unit l, 8 values in milliseconds from the start of that step:
- *   [8l+0] copy-in of master/m/v began   [8l+1] master landed
+ *   [8l+0] copy-in of master/m/v began   [8l+1] master landed (with the BF16
+ *                                        copy in HBM: the first chunk of master,
+ *                                        m and v landed)
  *   [8l+2] copy-in ended                 [8l+3] update kernel ended
  *   [8l+4] write-back began              [8l+5] write-back ended
  * (from events on the device), and, by the host clock from the moment the

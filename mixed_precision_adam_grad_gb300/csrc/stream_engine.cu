@@ -43,15 +43,17 @@
 //  forward sweep (H2D stream): the BF16 copy of unit l -> slot l%2, in order
 //                  (skipped when the copy is kept in HBM);
 //  reverse sweep, l = L-1 .. 0, slot s = l%2:
-//    H2D stream:     the master of l, then its m and v chunk by chunk; every
-//                    chunk first waits for the write-back of the same bytes by
-//                    the unit that used slot s before (l+2), so a slot is
-//                    handed over chunk by chunk;
-//    compute stream: once the master has landed, grad_fn(l) fills the R
-//                    replicas (backward's stand-in) and the clip pre-pass runs
-//                    over the whole unit; then the fused update of chunk k is
-//                    launched as soon as m_k and v_k have landed and the BF16
-//                    chunk of l+2 has been written back;
+//    H2D stream:     the master of l, then its m and v chunk by chunk (with
+//                    the BF16 copy in HBM: master, m and v interleaved chunk by
+//                    chunk); every chunk first waits for the write-back of the
+//                    same bytes by the unit that used slot s before (l+2), so
+//                    a slot is handed over chunk by chunk;
+//    compute stream: grad_fn(l) fills the R replicas (backward's stand-in) --
+//                    once the master has landed, as it reads the master; at
+//                    once with the BF16 copy in HBM, where it reads that copy --
+//                    and the clip pre-pass runs over the whole unit; then the
+//                    fused update of chunk k is launched as soon as its pieces
+//                    have landed and the BF16 chunk of l+2 has been written back;
 //    D2H stream:     the write-back of chunk k (BF16 copy, master, m, v)
 //                    follows its update, each piece recording the event that
 //                    the next copy-in to those bytes waits for.
@@ -371,12 +373,38 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
     if (e == cudaSuccess)
         e = cudaEventRecord(E->fwd_done, E->s_h2d);
 
-    // copy-in of master, m, v of unit l (H2D stream)
+    // copy-in of master, m, v of unit l (H2D stream).  With the BF16 copy in
+    // HBM the gradient callback reads that resident copy, not the master, so
+    // master, m and v arrive interleaved chunk by chunk and the update of chunk
+    // k waits only for its own three pieces; otherwise the whole master comes
+    // first (the callback reads it), then m and v chunk by chunk.
     auto copy_in = [&](int l) -> cudaError_t {
         Slot &s = E->slots[l % kSlots];
         const LayerState &U = st->layers[l];
         const int K = E->n_chunks(U.n);
         cudaError_t err = cudaEventRecord(E->h2d_begin[l], E->s_h2d);
+        if (!w_slot) {
+            for (int k = 0; k < K && err == cudaSuccess; ++k) {
+                const Chunk c = E->chunk(U.n, k);
+                const float *src[3] = {U.theta, U.m, U.v};
+                for (int r = 0; r < 3 && err == cudaSuccess; ++r) {
+                    err = E->wait_freed(E->s_h2d, s, r, c);
+                    if (err == cudaSuccess)
+                        err = cudaMemcpyAsync(s.arr[r] + c.off, src[r] + c.off, (size_t)c.len * 4,
+                                              cudaMemcpyHostToDevice, E->s_h2d);
+                }
+                if (err == cudaSuccess)
+                    err = cudaEventRecord(s.mv_landed[k], E->s_h2d);
+                if (err == cudaSuccess && k == 0)  // the first chunk: the update may start
+                    err = cudaEventRecord(E->theta_done[l], E->s_h2d);
+            }
+            if (err == cudaSuccess && K == 0)
+                err = cudaEventRecord(E->theta_done[l], E->s_h2d);
+            if (err == cudaSuccess)
+                err = cudaEventRecord(E->h2d_done[l], E->s_h2d);
+            E->host_copyin_enqueued[l] = host_ms();
+            return err;
+        }
         for (int k = 0; k < K && err == cudaSuccess; ++k) {
             const Chunk c = E->chunk(U.n, k);
             err = E->wait_freed(E->s_h2d, s, kTheta, c);
@@ -420,16 +448,21 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
             if (e != cudaSuccess)
                 break;
         }
-        // gradients of l as soon as its master has landed, then the clip
-        // pre-pass over the whole unit, then chunk by chunk the update
-        e = cudaStreamWaitEvent(E->s_comp, E->theta_done[l], 0);
-        if (e != cudaSuccess)
-            break;
+        // gradients of l (as soon as its master has landed, when the callback
+        // reads the master; at once when it reads the resident BF16 copy), then
+        // the clip pre-pass over the whole unit, then chunk by chunk the update
+        if (w_slot) {
+            e = cudaStreamWaitEvent(E->s_comp, E->theta_done[l], 0);
+            if (e != cudaSuccess)
+                break;
+        }
         if (U.n > 0) {
             void *reps[kMaxReplicas + 1];
             for (int r = 0; r < R; ++r)
                 reps[r] = s.g[r];
-            reps[R] = s.arr[0];  // the unit's FP32 master in the window (pre-update, read-only)
+            // the weights a backward pass reads, pre-update and read-only: the
+            // FP32 master in the window, or the unit's resident BF16 copy
+            reps[R] = w_slot ? (void *)s.arr[0] : (void *)U.w;
             int urc = fn(user, l, reps, (slide_stream_t)E->s_comp);
             if (urc != 0) {
                 rc = fail(SLIDE_ERR_ABORTED, "grad_fn returned " + std::to_string(urc) + " for unit " +

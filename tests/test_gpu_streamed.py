@@ -256,6 +256,53 @@ def test_streamed_python_callback_sees_master_and_errors_abort(S):
         S.slide_state_destroy(st)
 
 
+def test_streamed_callback_gets_resident_bf16_copy(S):
+    """With the BF16 copy kept in HBM the callback is handed each unit's
+    resident BF16 compute copy (what a backward pass reads there), holding
+    bf16 of the master before this step's update."""
+    sizes = [3000, 70001, 5000]
+    R = 2
+    st = S.slide_state_create(sizes, R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED, chunk_bytes=8192,
+                              flags=S.SLIDE_FLAG_BF16_COPY_IN_HBM)
+    seen = {}
+    snaps = {ui: torch.empty(n, dtype=torch.int16, device="cuda") for ui, n in enumerate(sizes)}
+
+    class DevView:
+        def __init__(self, ptr, n):
+            self.__cuda_array_interface__ = {"shape": (n,), "typestr": "<i2", "data": (ptr, False), "version": 2}
+
+    def cb(user, layer, ptrs, stream):
+        n = sizes[layer]
+        seen[layer] = ptrs[R]
+        # snapshot the weights handed over, on the callback's stream (before the update)
+        with torch.cuda.stream(torch.cuda.ExternalStream(stream)):
+            snaps[layer].copy_(torch.as_tensor(DevView(ptrs[R], n), device="cuda"))
+        for r in range(R):
+            synth.dev_grad(ptrs[r], n, synth.spec(1), layer, 1, r, 1e-3, stream=stream or 0)
+        return 0
+
+    fn = S.SLIDE_GRAD_FN(cb)
+    try:
+        masters = [synth.master(n, 4, unit=ui) for ui, n in enumerate(sizes)]
+        for ui in range(len(sizes)):
+            S.slide_layer_set(st, ui, master=masters[ui], step=0)
+        S.slide_model_step_streamed(st, fn, None, S.hparams())
+        assert sorted(seen) == [0, 1, 2]
+        for ui in seen:
+            assert seen[ui] == S.slide_layer_ptrs(st, ui)[3]
+            # the callback saw bf16 of the master before the update
+            assert np.array_equal(snaps[ui].cpu().numpy().view(np.uint16), oracle.f32_to_bf16(masters[ui]))
+        # after the step the resident copy is bf16 of the new master
+        for ui, n in enumerate(sizes):
+            th = np.empty(n, np.float32)
+            wb = np.empty(n, np.uint16)
+            S.slide_layer_get(st, ui, master=th, bf16=wb)
+            assert np.array_equal(wb, oracle.f32_to_bf16(th))
+            assert not np.array_equal(th, masters[ui])
+    finally:
+        S.slide_state_destroy(st)
+
+
 def test_streamed_version_gate(S):
     sizes = [100, 200]
     st = S.slide_state_create(sizes, 1, residency=S.SLIDE_RESIDENCY_HOST_STREAMED)
