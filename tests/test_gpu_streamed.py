@@ -109,10 +109,15 @@ def pinned_arena(nbytes):
     # write-back chunks smaller, larger and not a multiple of the copy-in chunks
     (0.0, 64 << 10, 4096, False, False, False), (0.5, 4096, 64 << 10, False, False, True),
     (0.0, 1024, 3072, True, True, True), (0.0, 768, 1 << 20, False, True, False),
-    (1e-3, 3072, 1024, False, False, True)])
+    (1e-3, 3072, 1024, False, False, True),
+    # the pinned state in a huge-page mapping registered with cudaHostRegister
+    (0.5, 64 << 10, 0, False, False, "huge"), (0.0, 4096, 64 << 10, False, True, "huge")])
 def test_streamed_toy_every_element(S, clip, chunk, chunk_d2h, fp32, in_hbm, arena):
     w = toy(clip=clip, fp32=fp32)
     flags = (S.SLIDE_FLAG_FP32_GRADS if fp32 else 0) | (S.SLIDE_FLAG_BF16_COPY_IN_HBM if in_hbm else 0)
+    if arena == "huge":
+        flags |= S.SLIDE_FLAG_HOST_HUGE_PAGES
+        arena = False
     sizes = [u.numel for u in w.units]
     keep, addr, nbytes = None, None, 0
     if arena:
