@@ -131,7 +131,8 @@ typedef struct {
     int64_t chunk_bytes;         /* streamed: host->device chunk of master, m and v, and the
                                     update's chunk (0 = 256 MiB); bytes of FP32, multiple of 256 */
     int64_t chunk_bytes_d2h;     /* streamed: device->host write-back chunk (0 = chunk_bytes);
-                                    bytes of FP32, multiple of 256 */
+                                    bytes of FP32, multiple of 256; both chunk sizes must cut
+                                    the largest unit into at most 65536 chunks */
     void *host_arena;            /* streamed: caller-owned pinned host memory (cudaHostAlloc, or
                                     cudaHostRegister with cudaHostRegisterMapped), 256-byte
                                     aligned, to hold the host state instead of an allocation of

@@ -121,6 +121,15 @@ static slide_status check_config(const slide_config *cfg, int64_t *max_numel)
         if (n > mx)
             mx = n;
     }
+    if (cfg->residency == SLIDE_RESIDENCY_HOST_STREAMED) {
+        // the engine keeps a few events per chunk and slot: bound the chunk count
+        const int64_t in = cfg->chunk_bytes > 0 ? cfg->chunk_bytes : ((int64_t)256 << 20);
+        const int64_t out = cfg->chunk_bytes_d2h > 0 ? cfg->chunk_bytes_d2h : in;
+        const int64_t bytes = mx * 4;
+        if ((bytes + in - 1) / in > kMaxChunksPerUnit || (bytes + out - 1) / out > kMaxChunksPerUnit)
+            return fail(SLIDE_ERR_INVALID_ARG, "config: chunk_bytes / chunk_bytes_d2h too small for the largest unit "
+                                               "(at most 65536 chunks per unit)");
+    }
     *max_numel = mx;
     return SLIDE_OK;
 }

@@ -69,6 +69,9 @@ void clear_error();
 AdamScalars adam_scalars_for(const slide_adam_hparams &hp, int64_t t);
 slide_status check_hparams(const slide_adam_hparams *hp);
 
+// Most copy-in or write-back chunks a streamed unit may have.
+constexpr int64_t kMaxChunksPerUnit = 65536;
+
 // Byte layout shared by slide_state_bytes and slide_state_create.
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }

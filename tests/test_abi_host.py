@@ -135,6 +135,8 @@ def test_accounting_streamed_bf16_copy_in_hbm(S):
     (dict(layer_numel=[10], n_replicas=1, flags=32), "flag"),
     (dict(layer_numel=[], n_replicas=1), "n_layers"),
     (dict(layer_numel=[10], n_replicas=1, chunk_bytes_d2h=100), "chunk_bytes_d2h"),
+    (dict(layer_numel=[1 << 26], n_replicas=1, residency=1, chunk_bytes=1024), "65536 chunks"),
+    (dict(layer_numel=[1 << 26], n_replicas=1, residency=1, chunk_bytes_d2h=2048), "65536 chunks"),
     (dict(layer_numel=[10], n_replicas=1, host_arena=1 << 20, host_arena_bytes=1 << 20), "streamed residency"),
     (dict(layer_numel=[10], n_replicas=1, residency=1, host_arena=(1 << 20) + 16, host_arena_bytes=1 << 20),
      "256-byte"),
