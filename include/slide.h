@@ -330,8 +330,9 @@ SLIDE_API slide_status slide_trace_events(slide_state *st, void *ev_prepass_star
  *   Errors: argument errors are returned before anything is enqueued.  A
  *   bounded wait inside the update kernel that runs out (2 s) leaves that
  *   step incomplete and marks the shared status word, which
- *   slide_noalloc_status reads.  Stream-ordered; returns before the GPU
- *   finishes. */
+ *   slide_noalloc_status reads (tests make that wait run out by setting the
+ *   environment variable SLIDE_TEST_PIPELINE_STALL).  Stream-ordered; returns
+ *   before the GPU finishes. */
 SLIDE_API slide_status slide_adamw_step_noalloc(int64_t n, int32_t n_replicas, const void *const *grad_replicas,
                                                 float *master, float *m, float *v, void *bf16_out,
                                                 const slide_adam_hparams *hp, int64_t step,

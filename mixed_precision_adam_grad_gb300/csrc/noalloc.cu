@@ -27,6 +27,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cstdlib>
 #include <mutex>
 #include <string>
 
@@ -138,8 +139,12 @@ extern "C" slide_status slide_adamw_step_noalloc(int64_t n, int32_t n_replicas, 
     }
     // with the clip off the kernel reads no partials (max_norm 0) but still
     // reports a wait that ran out into the status word
+    // SLIDE_TEST_PIPELINE_STALL (tests only): the update kernel's copy producer
+    // issues nothing, so the consumers' bounded wait (2 s) runs out and the
+    // status word reports it; the arrays are then undefined
+    const bool stall = getenv("SLIDE_TEST_PIPELINE_STALL") != nullptr;
     e = launch_grad_reduce_adamw_cast(g, n_replicas, n, master, m, v, (uint16_t *)bf16_out, sc, &cs,
-                                      n_partials, clip ? hp->max_grad_norm : 0.0f, false, device, s);
+                                      n_partials, clip ? hp->max_grad_norm : 0.0f, false, device, s, stall);
     if (e != cudaSuccess)
         return fail_cuda(e, "grad_reduce_adamw_cast launch (no-alloc)");
     clear_error();

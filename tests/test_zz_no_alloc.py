@@ -121,6 +121,42 @@ def test_noalloc_allocates_nothing_after_setup(S):
     assert np.isfinite(th.cpu().numpy()).all()
 
 
+def test_noalloc_status_reports_a_wait_that_ran_out(S, monkeypatch):
+    """A bounded wait inside the update kernel that runs out is reported once
+    by slide_noalloc_status, which clears it; the next call is correct again.
+    The wait is made to run out on purpose (test-only switch: the kernel's copy
+    producer issues nothing), with no fault and no unbounded wait."""
+    n, R, seed = 70_001, 2, 13
+    sp = synth.spec(seed)
+    grads = [torch.empty(n + 64, dtype=torch.int16, device="cuda") for _ in range(R)]
+    for r in range(R):
+        synth.dev_grad(grads[r].data_ptr(), n, sp, 0, 1, r, 1e-3)
+    th = torch.from_numpy(synth.master(n, seed)).cuda()
+    m = torch.zeros(n, dtype=torch.float32, device="cuda")
+    v = torch.zeros(n, dtype=torch.float32, device="cuda")
+    w = torch.zeros(n + 8, dtype=torch.int16, device="cuda")
+    hp = S.hparams(max_grad_norm=1.0)
+    assert S.slide_noalloc_status() == S.SLIDE_OK
+    monkeypatch.setenv("SLIDE_TEST_PIPELINE_STALL", "1")
+    S.slide_adamw_step_noalloc(n, grads, th, m, v, w, hp, 1)
+    monkeypatch.delenv("SLIDE_TEST_PIPELINE_STALL")
+    assert S.slide_noalloc_status() == S.SLIDE_ERR_TIMEOUT
+    assert S.slide_noalloc_status() == S.SLIDE_OK      # read and cleared
+    # the caller restores its arrays and steps again: as the oracle
+    th.copy_(torch.from_numpy(synth.master(n, seed)))
+    m.zero_()
+    v.zero_()
+    S.slide_adamw_step_noalloc(n, grads, th, m, v, w, hp, 1)
+    assert S.slide_noalloc_status() == S.SLIDE_OK
+    o_th, o_m, o_v = synth.master(n, seed), np.zeros(n, np.float32), np.zeros(n, np.float32)
+    o_w = np.zeros(n, np.uint16)
+    oracle.layer_step([synth.grad(n, sp, 0, 1, r, 1e-3) for r in range(R)], o_th, o_m, o_v, o_w,
+                      oracle.hparams(max_grad_norm=1.0), 1)
+    pu.assert_parity([pu.compare_fp32("theta", th.cpu().numpy(), o_th), pu.compare_fp32("m", m.cpu().numpy(), o_m),
+                      pu.compare_fp32("v", v.cpu().numpy(), o_v),
+                      pu.compare_bf16("w", w[:n].cpu().numpy().view(np.uint16), o_w)])
+
+
 def test_noalloc_rejects_out_of_range(S):
     g = [torch.zeros(64, dtype=torch.int16, device="cuda")]
     x = torch.zeros(64, dtype=torch.float32, device="cuda")
