@@ -895,7 +895,7 @@ def run_ours(args):
             print(f"detail {json.dumps({'pinned_arena_unavailable': str(exc)})}", flush=True)
             arena = None
 
-    st = S.slide_state_create([n], R, device=local)
+    st = S.slide_state_create([n], R, device=local, flags=0 if args.no_e2e else S.SLIDE_FLAG_HOST_INPUTS)
     try:
         th_d = S.slide_layer_ptrs(st, 0)[0]
         synth.dev_master(th_d, n, w.seed + 100 * rank, stream=stream.cuda_stream)
@@ -959,11 +959,12 @@ def run_ours(args):
         upd_ms = [e[1].elapsed_time(e[2]) for e in ev]
         ms_total = max_over_ranks(ms_total, dist)
 
-        # End to end through the public API: every step copies its R replicas
-        # from pinned host memory into the GPU and its BF16 copy back to pinned
-        # host memory.  Pipelined as a user would: two device replica buffers;
-        # the copy-in of step k+1 (copy stream) overlaps the update and the
-        # copy-out of step k (compute stream), ordered by events.
+        # End to end through the C ABI with host buffers: every step is one
+        # slide_layer_step_host call on the step's R replicas in pinned host
+        # memory and a pinned host buffer for its BF16 copy.  The library copies
+        # the replicas into one of its two device staging sets on its copy
+        # stream (the copy-in of step k+1 overlaps the update of step k), runs
+        # the step behind the copy and copies the BF16 copy back on `stream`.
         e2e = None
         if not args.no_e2e:
             Ke = max(3, min(args.e2e_steps, K))
@@ -972,58 +973,29 @@ def run_ours(args):
             for b in range(2):
                 for r in range(R):
                     host_reps[b][r].copy_(batches[b % len(batches)][r][:n])
-            dev_reps = [[torch.empty(n + 64, dtype=torch.int16, device="cuda") for _ in range(R)] for _ in range(2)]
-            out_dev = [torch.empty(n + 64, dtype=torch.int16, device="cuda") for _ in range(2)]
             out_host = [alloc(n, torch.int16) for _ in range(2)]
-            copy_stream = torch.cuda.Stream()
-            landed = [torch.cuda.Event() for _ in range(2)]
-            consumed = [torch.cuda.Event() for _ in range(2)]
             torch.cuda.synchronize()
 
-            def copy_in(k):
-                b = k % 2
-                copy_stream.wait_event(consumed[b])          # the step that read this buffer is done
-                with torch.cuda.stream(copy_stream):
-                    for r in range(R):
-                        dev_reps[b][r][:n].copy_(host_reps[b][r], non_blocking=True)
-                    landed[b].record(copy_stream)
-
-            def step_out(k):
-                b = k % 2
-                stream.wait_event(landed[b])
-                S.slide_layer_step(st, 0, dev_reps[b], hp, stream, out_dev[b])
-                consumed[b].record(stream)
-                with torch.cuda.stream(stream):
-                    out_host[b].copy_(out_dev[b][:n], non_blocking=True)
-
             def run_e2e(steps):
-                copy_in(0)
                 for k in range(steps):
-                    if k + 1 < steps:
-                        copy_in(k + 1)
-                    step_out(k)
+                    S.slide_layer_step_host(st, 0, host_reps[k % 2], hp, stream, out_host[k % 2])
 
-            for e in consumed:
-                e.record(stream)
             run_e2e(3)
             torch.cuda.synchronize()
             if dist:
                 dist.barrier()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            copy_stream.wait_event(e0)
             run_e2e(Ke)
-            copy_stream_done = torch.cuda.Event()
-            copy_stream_done.record(copy_stream)
-            stream.wait_event(copy_stream_done)
-            e1.record(stream)
+            e1.record(stream)        # behind the last step's copy-out, which is behind its copy-in
             torch.cuda.synchronize()
             ms_e2e = e0.elapsed_time(e1)
             ms_e2e = max_over_ranks(ms_e2e, dist)
             e2e = {"value": n * Ke * world / (ms_e2e * 1e-3) / 1e9, "unit": UNIT,
                    "h2d_bytes_per_step": 2 * R * n, "d2h_bytes_per_step": 2 * n, "steps": Ke,
-                   "pipelining": "copy-in of step k+1 on a copy stream overlaps step k's update and copy-out"}
-            del host_reps, out_host, dev_reps, out_dev
+                   "call": "slide_layer_step_host (host replicas in, host BF16 copy out)",
+                   "pipelining": "the library's copy stream: the copy-in of step k+1 overlaps step k's update"}
+            del host_reps, out_host
             if arena is not None:
                 arena.reset()
     finally:

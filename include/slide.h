@@ -104,6 +104,9 @@ enum {
                                             unit's resident copy in place: the copy is neither
                                             delivered nor written back, and the window has no BF16
                                             buffers) */
+    SLIDE_FLAG_HOST_INPUTS = 32u,        /* HBM residency: reserve device staging for
+                                            slide_layer_step_host (two sets of R replica buffers for
+                                            the largest layer, used in turn) and a copy stream */
     SLIDE_FLAG_HOST_HUGE_PAGES = 16u     /* streamed residency: back the pinned host state with an
                                             anonymous mapping advised for transparent huge pages and
                                             pinned with cudaHostRegister, instead of cudaHostAlloc
@@ -209,6 +212,31 @@ SLIDE_API slide_status slide_state_bytes(const slide_config *cfg, int64_t *devic
  * The clip is the workload's; the pages describe none. */
 SLIDE_API slide_status slide_layer_step(slide_state *st, int32_t layer, const void *const *grad_replicas,
                               const slide_adam_hparams *hp, slide_stream_t stream, void *bf16_out);
+
+/* One optimizer step of one layer whose gradient replicas are in host memory
+ * and whose new BF16 copy is wanted in host memory (HBM residency, state
+ * created with SLIDE_FLAG_HOST_INPUTS): the R replicas are copied into the
+ * next of the state's two device staging sets on the state's own copy stream,
+ * the step of slide_layer_step runs on `stream` behind that copy, and the new
+ * BF16 copy is copied back to host_bf16_out on `stream` (skipped if NULL).
+ *   host_grad_replicas: host array of R host pointers (pinned for asynchronous
+ *     copies; pageable works, synchronously), each to layer_numel[layer] BF16
+ *     values (FP32 with SLIDE_FLAG_FP32_GRADS).  They must hold the gradients
+ *     when the call is made (the copy does not wait for work on `stream`) and
+ *     stay valid until the copy has run.
+ *   host_bf16_out: host pointer receiving layer_numel[layer] BF16 values, or
+ *     NULL; valid until `stream` has passed the copy.
+ * The copy into a staging set waits only for the update that last read it, so
+ * the copy-in of one call overlaps the update of the previous one.
+ * Stream-ordered; returns before the GPU finishes.  Calls for one state must
+ * come from one host thread.
+ * Defined by: the passages of slide_layer_step; the copies are the transfer
+ * step of "SlideDP: Scaling Host-Resident LLM Fine-Tuning Across Multiple
+ * GPUs", Method steps (backward -> reduce -> transfer -> Adam), with the
+ * gradients arriving from host memory. */
+SLIDE_API slide_status slide_layer_step_host(slide_state *st, int32_t layer, const void *const *host_grad_replicas,
+                                             const slide_adam_hparams *hp, slide_stream_t stream,
+                                             void *host_bf16_out);
 
 /* One synchronous step of every unit of a host-streamed state (residency
  * SLIDE_RESIDENCY_HOST_STREAMED).  Requires every unit's t to be equal on

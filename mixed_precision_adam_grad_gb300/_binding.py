@@ -38,6 +38,7 @@ SLIDE_FLAG_TEST_PIPELINE_STALL = 2
 SLIDE_FLAG_FP32_GRADS = 4
 SLIDE_FLAG_BF16_COPY_IN_HBM = 8
 SLIDE_FLAG_HOST_HUGE_PAGES = 16
+SLIDE_FLAG_HOST_INPUTS = 32
 SLIDE_MAX_REPLICAS = 8
 SLIDE_DELIVER_FULL = 0
 SLIDE_DELIVER_SHARDED = 1
@@ -80,6 +81,8 @@ def _load():
     L.slide_state_bytes.restype = S
     L.slide_layer_step.argtypes = [P, C.c_int32, C.POINTER(C.c_void_p), C.POINTER(slide_adam_hparams), P, P]
     L.slide_layer_step.restype = S
+    L.slide_layer_step_host.argtypes = [P, C.c_int32, C.POINTER(C.c_void_p), C.POINTER(slide_adam_hparams), P, P]
+    L.slide_layer_step_host.restype = S
     L.slide_model_step_streamed.argtypes = [P, P, P, C.POINTER(slide_adam_hparams)]
     L.slide_model_step_streamed.restype = S
     L.slide_layer_set.argtypes = [P, C.c_int32, P, P, P, C.c_int64]
@@ -229,6 +232,16 @@ def slide_layer_step(st: SlideState, layer: int, grad_replicas, hp: slide_adam_h
     arr = (C.c_void_p * max(1, len(ptrs)))(*ptrs)
     _check(_lib().slide_layer_step(C.c_void_p(st.handle), layer, arr, C.byref(hp),
                                 _stream(stream), _ptr(bf16_out)))
+
+
+def slide_layer_step_host(st: SlideState, layer: int, host_grad_replicas, hp: slide_adam_hparams,
+                          stream=None, host_bf16_out=None) -> None:
+    """The step of a layer whose replicas are host arrays (numpy arrays, pinned
+    CPU tensors or addresses); the new BF16 copy goes to host_bf16_out."""
+    ptrs = [_ptr(g) for g in host_grad_replicas]
+    arr = (C.c_void_p * max(1, len(ptrs)))(*ptrs)
+    _check(_lib().slide_layer_step_host(C.c_void_p(st.handle), layer, arr, C.byref(hp), _stream(stream),
+                                        _ptr(host_bf16_out)))
 
 
 def slide_model_step_streamed(st: SlideState, fn, user, hp: slide_adam_hparams) -> None:

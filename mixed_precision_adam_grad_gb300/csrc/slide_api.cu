@@ -11,6 +11,7 @@
 // one arena allocation, allocated once at creation (no allocation on the
 // step path).
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExtCudaRt.h>
 
 #include <sys/mman.h>
 
@@ -109,8 +110,10 @@ static slide_status check_config(const slide_config *cfg, int64_t *max_numel)
         return fail(SLIDE_ERR_INVALID_ARG, "config: host_arena_bytes without a host_arena");
     }
     if (cfg->flags & ~(uint32_t)(SLIDE_FLAG_CHECK_FINITE | SLIDE_FLAG_TEST_PIPELINE_STALL | SLIDE_FLAG_FP32_GRADS |
-                                 SLIDE_FLAG_BF16_COPY_IN_HBM | SLIDE_FLAG_HOST_HUGE_PAGES))
+                                 SLIDE_FLAG_BF16_COPY_IN_HBM | SLIDE_FLAG_HOST_HUGE_PAGES | SLIDE_FLAG_HOST_INPUTS))
         return fail(SLIDE_ERR_INVALID_ARG, "config: unknown flag bits");
+    if ((cfg->flags & SLIDE_FLAG_HOST_INPUTS) && cfg->residency != SLIDE_RESIDENCY_HBM)
+        return fail(SLIDE_ERR_INVALID_ARG, "config: SLIDE_FLAG_HOST_INPUTS is for the HBM residency");
     if (cfg->device < 0)
         return fail(SLIDE_ERR_INVALID_ARG, "config: device < 0");
     int64_t mx = 0;
@@ -168,7 +171,7 @@ slide_status slide_state_bytes(const slide_config *cfg, int64_t *device_bytes, i
         state += layer_state_bytes(cfg->layer_numel[l]);
     size_t dev = 0, host = 0;
     if (cfg->residency == SLIDE_RESIDENCY_HBM) {
-        dev = state + (size_t)cfg->n_layers * scratch_bytes();
+        dev = state + (size_t)cfg->n_layers * scratch_bytes() + host_input_bytes(*cfg, mx);
     } else if (copy_in_hbm(cfg)) {
         for (int32_t l = 0; l < cfg->n_layers; ++l) {
             host += layer_fp32_bytes(cfg->layer_numel[l]);
@@ -257,6 +260,56 @@ static void host_arena_free(slide_state *st)
     st->host_map_bytes = 0;
 }
 
+static void host_inputs_destroy(slide_state *st)
+{
+    HostInputs *H = st->hin;
+    if (!H)
+        return;
+    if (H->copy)
+        cudaStreamSynchronize(H->copy);
+    for (int b = 0; b < 2; ++b) {
+        if (H->landed[b])
+            cudaEventDestroy(H->landed[b]);
+        if (H->consumed[b])
+            cudaEventDestroy(H->consumed[b]);
+    }
+    if (H->copy)
+        cudaStreamDestroy(H->copy);
+    delete H;
+    st->hin = nullptr;
+}
+
+// The staging of slide_layer_step_host in the device arena at `base` (2 sets
+// x R replicas of max_numel values), its copy stream and events.
+static slide_status host_inputs_create(slide_state *st, char *base, int64_t max_numel)
+{
+    HostInputs *H = new (std::nothrow) HostInputs();
+    if (!H)
+        return fail(SLIDE_ERR_OOM_HOST, "out of host memory for the host-input staging");
+    st->hin = H;
+    const size_t g = (st->cfg.flags & SLIDE_FLAG_FP32_GRADS) ? 4 : 2;
+    const size_t per = align_up((size_t)max_numel * g);
+    for (int b = 0; b < 2; ++b)
+        for (int r = 0; r < st->cfg.n_replicas; ++r) {
+            H->stage[b][r] = base;
+            base += per;
+        }
+    cudaError_t e = cudaStreamCreateWithFlags(&H->copy, cudaStreamNonBlocking);
+    for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+        e = cudaEventCreateWithFlags(&H->landed[b], cudaEventDisableTiming);
+        if (e == cudaSuccess)
+            e = cudaEventCreateWithFlags(&H->consumed[b], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) {
+        slide_status rc = fail_cuda(e, "host-input staging set-up");
+        host_inputs_destroy(st);
+        return rc;
+    }
+    if (e == cudaSuccess)
+        nvtxNameCudaStreamA(H->copy, "slide host-input copy");
+    return SLIDE_OK;
+}
+
 slide_status slide_state_create(const slide_config *cfg, slide_state **out)
 {
     if (!out)
@@ -298,7 +351,7 @@ slide_status slide_state_create(const slide_config *cfg, slide_state **out)
 
     char *base = nullptr;
     if (cfg->residency == SLIDE_RESIDENCY_HBM) {
-        st->dev_bytes = state_bytes + (size_t)cfg->n_layers * scratch_bytes();
+        st->dev_bytes = state_bytes + (size_t)cfg->n_layers * scratch_bytes() + host_input_bytes(*cfg, mx);
         e = cudaMalloc(&st->dev_arena, st->dev_bytes);
         if (e != cudaSuccess) {
             cudaGetLastError();
@@ -406,6 +459,14 @@ slide_status slide_state_create(const slide_config *cfg, slide_state **out)
             L.scratch.status = (unsigned *)(L.scratch.coef + 1);
             off += scratch_bytes();
         }
+        if (cfg->flags & SLIDE_FLAG_HOST_INPUTS) {
+            rc = host_inputs_create(st, base + off, mx);
+            if (rc != SLIDE_OK) {
+                cudaFree(st->dev_arena);
+                delete st;
+                return rc;
+            }
+        }
     } else {
         rc = engine_create(st);
         if (rc != SLIDE_OK) {
@@ -428,6 +489,7 @@ void slide_state_destroy(slide_state *st)
     DeviceGuard guard(st->device);
     if (st->engine)
         engine_destroy(st);
+    host_inputs_destroy(st);
     if (st->dev_arena) {
         cudaDeviceSynchronize();
         cudaFree(st->dev_arena);
@@ -442,6 +504,45 @@ static slide_status check_layer(slide_state *st, int32_t layer)
         return fail(SLIDE_ERR_INVALID_ARG, "state is NULL");
     if (layer < 0 || layer >= (int32_t)st->layers.size())
         return fail(SLIDE_ERR_INVALID_ARG, "layer index out of range");
+    return SLIDE_OK;
+}
+
+// Enqueue the step of one layer (clip pre-pass if on, then the fused kernel)
+// on s, reading the replicas g and writing the BF16 copy to w; the device is
+// current.  `after_update`, if given, is recorded behind the fused kernel.
+static slide_status enqueue_layer_step(slide_state *st, LayerState &L, const ReplicaPtrs &g,
+                                       const slide_adam_hparams *hp, cudaStream_t s, uint16_t *w,
+                                       cudaEvent_t after_update)
+{
+    const int R = st->cfg.n_replicas;
+    const int64_t t = L.t + 1;
+    {
+        const AdamScalars sc = adam_scalars_for(*hp, t);
+        const bool clip = hp->max_grad_norm > 0.0f;
+        const bool check = (st->cfg.flags & SLIDE_FLAG_CHECK_FINITE) != 0;
+        int n_partials = 0;
+        cudaError_t e;
+        if (st->trace[0])
+            cudaEventRecord(st->trace[0], s);
+        const bool f32g = (st->cfg.flags & SLIDE_FLAG_FP32_GRADS) != 0;
+        if (clip) {
+            e = launch_grad_sqnorm(g, R, L.n, L.scratch, &n_partials, st->device, s, f32g);
+            if (e != cudaSuccess)
+                return fail_cuda(e, "grad_sqnorm launch");
+        }
+        if (st->trace[1])
+            cudaEventRecord(st->trace[1], s);
+        e = launch_grad_reduce_adamw_cast(g, R, L.n, L.theta, L.m, L.v, w, sc, &L.scratch, n_partials,
+                                          clip ? hp->max_grad_norm : 0.0f, check, st->device, s,
+                                          (st->cfg.flags & SLIDE_FLAG_TEST_PIPELINE_STALL) != 0, f32g);
+        if (e != cudaSuccess)
+            return fail_cuda(e, "grad_reduce_adamw_cast launch");
+        if (after_update && (e = cudaEventRecord(after_update, s)) != cudaSuccess)
+            return fail_cuda(e, "event record after the update");
+        if (st->trace[2])
+            cudaEventRecord(st->trace[2], s);
+    }
+    L.t = t;
     return SLIDE_OK;
 }
 
@@ -468,37 +569,72 @@ slide_status slide_layer_step(slide_state *st, int32_t layer, const void *const 
     uint16_t *w = bf16_out ? (uint16_t *)bf16_out : L.w;
     if (!aligned16(w))
         return fail(SLIDE_ERR_INVALID_ARG, "bf16_out is not 16-byte aligned");
-
-    const int64_t t = L.t + 1;
-    if (L.n > 0) {
-        DeviceGuard guard(st->device);
-        if (!guard.ok)
-            return fail(SLIDE_ERR_CUDA, "cudaSetDevice failed");
-        cudaStream_t s = (cudaStream_t)stream;
-        const AdamScalars sc = adam_scalars_for(*hp, t);
-        const bool clip = hp->max_grad_norm > 0.0f;
-        const bool check = (st->cfg.flags & SLIDE_FLAG_CHECK_FINITE) != 0;
-        int n_partials = 0;
-        cudaError_t e;
-        if (st->trace[0])
-            cudaEventRecord(st->trace[0], s);
-        const bool f32g = (st->cfg.flags & SLIDE_FLAG_FP32_GRADS) != 0;
-        if (clip) {
-            e = launch_grad_sqnorm(g, R, L.n, L.scratch, &n_partials, st->device, s, f32g);
-            if (e != cudaSuccess)
-                return fail_cuda(e, "grad_sqnorm launch");
-        }
-        if (st->trace[1])
-            cudaEventRecord(st->trace[1], s);
-        e = launch_grad_reduce_adamw_cast(g, R, L.n, L.theta, L.m, L.v, w, sc, &L.scratch, n_partials,
-                                          clip ? hp->max_grad_norm : 0.0f, check, st->device, s,
-                                          (st->cfg.flags & SLIDE_FLAG_TEST_PIPELINE_STALL) != 0, f32g);
-        if (e != cudaSuccess)
-            return fail_cuda(e, "grad_reduce_adamw_cast launch");
-        if (st->trace[2])
-            cudaEventRecord(st->trace[2], s);
+    if (L.n == 0) {
+        L.t += 1;
+        clear_error();
+        return SLIDE_OK;
     }
-    L.t = t;
+    DeviceGuard guard(st->device);
+    if (!guard.ok)
+        return fail(SLIDE_ERR_CUDA, "cudaSetDevice failed");
+    rc = enqueue_layer_step(st, L, g, hp, (cudaStream_t)stream, w, nullptr);
+    if (rc == SLIDE_OK)
+        clear_error();
+    return rc;
+}
+
+slide_status slide_layer_step_host(slide_state *st, int32_t layer, const void *const *host_grad_replicas,
+                                   const slide_adam_hparams *hp, slide_stream_t stream, void *host_bf16_out)
+{
+    slide_status rc = check_layer(st, layer);
+    if (rc != SLIDE_OK)
+        return rc;
+    if (st->cfg.residency != SLIDE_RESIDENCY_HBM || !st->hin)
+        return fail(SLIDE_ERR_STATE, "slide_layer_step_host needs the HBM residency and SLIDE_FLAG_HOST_INPUTS");
+    if ((rc = check_hparams(hp)) != SLIDE_OK)
+        return rc;
+    LayerState &L = st->layers[layer];
+    const int R = st->cfg.n_replicas;
+    if (!host_grad_replicas)
+        return fail(SLIDE_ERR_INVALID_ARG, "host_grad_replicas is NULL");
+    for (int r = 0; r < R; ++r)
+        if (L.n > 0 && !host_grad_replicas[r])
+            return fail(SLIDE_ERR_INVALID_ARG, "a host gradient replica pointer is NULL");
+    if (L.n == 0) {
+        L.t += 1;
+        clear_error();
+        return SLIDE_OK;
+    }
+    DeviceGuard guard(st->device);
+    if (!guard.ok)
+        return fail(SLIDE_ERR_CUDA, "cudaSetDevice failed");
+    HostInputs &H = *st->hin;
+    const int b = H.next;
+    const size_t gbytes = (size_t)L.n * ((st->cfg.flags & SLIDE_FLAG_FP32_GRADS) ? 4 : 2);
+    cudaStream_t s = (cudaStream_t)stream;
+    // copy-in on the state's copy stream, once the update that last read this
+    // staging set is done; the caller's stream waits for it to land
+    cudaError_t e = cudaStreamWaitEvent(H.copy, H.consumed[b], 0);
+    ReplicaPtrs g{};
+    for (int r = 0; r < R && e == cudaSuccess; ++r) {
+        g.p[r] = H.stage[b][r];
+        e = cudaMemcpyAsync(H.stage[b][r], host_grad_replicas[r], gbytes, cudaMemcpyHostToDevice, H.copy);
+    }
+    if (e == cudaSuccess)
+        e = cudaEventRecord(H.landed[b], H.copy);
+    if (e == cudaSuccess)
+        e = cudaStreamWaitEvent(s, H.landed[b], 0);
+    if (e != cudaSuccess)
+        return fail_cuda(e, "copy-in of the host gradient replicas");
+    H.next = b ^ 1;
+    rc = enqueue_layer_step(st, L, g, hp, s, L.w, H.consumed[b]);
+    if (rc != SLIDE_OK)
+        return rc;
+    if (host_bf16_out) {
+        e = cudaMemcpyAsync(host_bf16_out, L.w, (size_t)L.n * 2, cudaMemcpyDeviceToHost, s);
+        if (e != cudaSuccess)
+            return fail_cuda(e, "copy-out of the BF16 copy");
+    }
     clear_error();
     return SLIDE_OK;
 }

@@ -14,6 +14,17 @@ namespace slide {
 
 struct StreamEngine;  // stream_engine.cu
 
+// Device staging of slide_layer_step_host (SLIDE_FLAG_HOST_INPUTS): two sets
+// of R replica buffers for the largest layer, used in turn, a copy stream for
+// the copy-in and, per set, "landed" and "consumed" (updated) events.
+struct HostInputs {
+    void *stage[2][kMaxReplicas] = {};
+    cudaStream_t copy = nullptr;
+    cudaEvent_t landed[2] = {nullptr, nullptr};
+    cudaEvent_t consumed[2] = {nullptr, nullptr};
+    int next = 0;
+};
+
 struct LayerState {
     int64_t n = 0;
     float *theta = nullptr;  // HBM or pinned host (streamed)
@@ -54,6 +65,7 @@ struct slide_state {
     size_t host_map_bytes = 0;   // > 0: host_arena is a registered mapping of this length (huge pages)
     bool host_arena_owned = true;  // false: host_arena is the caller's (never freed here)
     slide::StreamEngine *engine = nullptr;
+    slide::HostInputs *hin = nullptr;  // SLIDE_FLAG_HOST_INPUTS
     bool aborted = false;
     cudaEvent_t trace[3] = {nullptr, nullptr, nullptr};  // prepass start, update start, update stop
 };
@@ -76,6 +88,14 @@ constexpr int64_t kMaxChunksPerUnit = 65536;
 constexpr size_t kAlign = 256;
 inline size_t align_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 inline size_t scratch_bytes() { return align_up(sizeof(double) * kMaxPartials) + kAlign; }
+// Staging of SLIDE_FLAG_HOST_INPUTS: 2 sets x R replicas of the largest layer.
+inline size_t host_input_bytes(const slide_config &cfg, int64_t max_numel)
+{
+    if (!(cfg.flags & SLIDE_FLAG_HOST_INPUTS))
+        return 0;
+    const size_t g = (cfg.flags & SLIDE_FLAG_FP32_GRADS) ? 4 : 2;
+    return 2 * (size_t)cfg.n_replicas * align_up((size_t)max_numel * g);
+}
 
 // Streamed residency (stream_engine.cu).
 slide_status engine_create(slide_state *st);

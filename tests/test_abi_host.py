@@ -97,6 +97,18 @@ def test_accounting_16N(S):
     assert state_per_param * N <= dev - len(sizes) * scratch <= state_per_param * N + 4 * A * len(sizes)
 
 
+def test_accounting_host_inputs_staging(S):
+    """SLIDE_FLAG_HOST_INPUTS adds two staging sets of R replicas of the
+    largest layer (BF16, or FP32 with SLIDE_FLAG_FP32_GRADS)."""
+    sizes = [1000, 70001, 17]
+    for R, fp32, g in ((3, False, 2), (4, True, 4)):
+        f = S.SLIDE_FLAG_FP32_GRADS if fp32 else 0
+        base, _ = S.slide_state_bytes(sizes, R, flags=f)
+        with_in, host = S.slide_state_bytes(sizes, R, flags=f | S.SLIDE_FLAG_HOST_INPUTS)
+        assert host == 0
+        assert with_in - base == 2 * R * al(g * max(sizes))
+
+
 def test_accounting_streamed_window_independent_of_N(S):
     one = [330_311_680]
     many = [778_567_680] + [330_311_680] * 40 + [778_567_680]
@@ -132,7 +144,8 @@ def test_accounting_streamed_bf16_copy_in_hbm(S):
     (dict(layer_numel=[10], n_replicas=1, residency=7), "residency"),
     (dict(layer_numel=[10], n_replicas=1, chunk_bytes=100), "chunk_bytes"),
     (dict(layer_numel=[10], n_replicas=1, window_layers=3), "window_layers"),
-    (dict(layer_numel=[10], n_replicas=1, flags=32), "flag"),
+    (dict(layer_numel=[10], n_replicas=1, flags=64), "flag"),
+    (dict(layer_numel=[10], n_replicas=1, residency=1, flags=32), "HBM residency"),
     (dict(layer_numel=[], n_replicas=1), "n_layers"),
     (dict(layer_numel=[10], n_replicas=1, chunk_bytes_d2h=100), "chunk_bytes_d2h"),
     (dict(layer_numel=[1 << 26], n_replicas=1, residency=1, chunk_bytes=1024), "65536 chunks"),
