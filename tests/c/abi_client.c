@@ -103,6 +103,28 @@ static int gpu_checks(void)
     for (int r = 0; r < R; ++r)
         cudaFree(grads[r]);
     slide_state_destroy(st);
+
+    /* the same closed form with the gradients in host memory and the BF16
+     * copy delivered to host memory: slide_layer_step_host */
+    cfg.flags = SLIDE_FLAG_HOST_INPUTS;
+    CHECK(slide_state_create(&cfg, &st) == SLIDE_OK && st, "slide_state_create (host inputs)");
+    CHECK(slide_layer_set(st, 0, th0, NULL, NULL, 0) == SLIDE_OK, "slide_layer_set (host inputs)");
+    uint16_t *hg[2] = {calloc(n, 2), calloc(n, 2)};
+    uint16_t *wout = malloc(n * sizeof(uint16_t));
+    const void *hptr[2] = {hg[0], hg[1]};
+    for (int k = 1; k <= 3; ++k)
+        CHECK(slide_layer_step_host(st, 0, hptr, &hp, NULL, wout) == SLIDE_OK, "host step %d", k);
+    CHECK(cudaDeviceSynchronize() == cudaSuccess, "sync");
+    CHECK(slide_layer_get(st, 0, th, m, v, w, &t) == SLIDE_OK && t == 3, "slide_layer_get / t (host inputs)");
+    for (int64_t i = 0; i < n; ++i) {
+        float e = th0[i];
+        for (int k = 0; k < 3; ++k)
+            e = e * decay;
+        CHECK(th[i] == e, "host inputs: theta[%lld] = %.9g, want %.9g", (long long)i, th[i], e);
+        CHECK(wout[i] == to_bf16(e), "host inputs: delivered bf16 copy at %lld", (long long)i);
+    }
+    slide_state_destroy(st);
+    free(hg[0]), free(hg[1]), free(wout);
     free(th0), free(th), free(m), free(v), free(w);
     return 0;
 }

@@ -1,8 +1,8 @@
 """A plain C program uses the C ABI: it includes include/slide.h, links
 libslide.so and the CUDA runtime, and calls the entry points directly (no
 Python, no torch).  Host-only calls run without a GPU; the GPU part checks a
-closed form (zero gradients from zero moments: pure decay) and that a refused
-call changes nothing."""
+closed form (zero gradients from zero moments: pure decay) with device and
+with host gradient buffers, and that a refused call changes nothing."""
 import os
 import subprocess
 
