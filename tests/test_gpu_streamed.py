@@ -158,6 +158,35 @@ def test_streamed_toy_every_element(S, clip, chunk, chunk_d2h, fp32, in_hbm, are
         S.slide_state_destroy(st)
 
 
+@pytest.mark.parametrize("sizes,in_hbm", [([123_457], False), ([123_457], True), ([0, 70_001], False),
+                                           ([70_001, 0], True), ([5, 3], False)])
+def test_streamed_few_units_every_element(S, sizes, in_hbm):
+    """Models of one or two units (one of them empty, or both tiny): the slot
+    handoff with no neighbour, every element against the oracle for 3 steps."""
+    w = W.Workload("few", [W.Unit(f"u{i}", [("a", n)]) for i, n in enumerate(sizes)], R=3, steps=3, seed=23,
+                   max_grad_norm=0.5, lr=1e-3, streamed=True)
+    flags = S.SLIDE_FLAG_BF16_COPY_IN_HBM if in_hbm else 0
+    st = S.slide_state_create(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED, chunk_bytes=4096, flags=flags)
+    try:
+        init_streamed(S, w, st)
+        ref = [[synth.master(n, w.seed, unit=ui), np.zeros(n, np.float32), np.zeros(n, np.float32),
+                np.zeros(n, np.uint16)] for ui, n in enumerate(sizes)]
+        hp = S.hparams(*w.hparams_tuple())
+        for t in range(1, w.steps + 1):
+            holder = ModelGradsHolder(w, t)
+            S.slide_model_step_streamed(st, synth.grad_fn_address(), holder.mg, hp)
+            for ui, n in enumerate(sizes):
+                oracle.layer_step([pu.unit_grad_host(w, ui, t, r) for r in range(w.R)], *ref[ui], pu.hp_oracle(w), t)
+        for ui, n in enumerate(sizes):
+            a, b, c = (np.empty(n, np.float32) for _ in range(3))
+            wb = np.empty(n, np.uint16)
+            assert S.slide_layer_get(st, ui, a, b, c, wb) == w.steps
+            pu.assert_parity([pu.compare_fp32("theta", a, ref[ui][0]), pu.compare_fp32("m", b, ref[ui][1]),
+                              pu.compare_fp32("v", c, ref[ui][2]), pu.compare_bf16("w", wb, ref[ui][3])])
+    finally:
+        S.slide_state_destroy(st)
+
+
 def test_streamed_caller_arena_reused_by_states(S):
     """One caller-owned pinned arena serves two states in turn: the first
     state's steps leave it dirty, the second starts from zero state (the
