@@ -801,6 +801,19 @@ def run_streamed(args, S, torch, synth, key, arena=None):
             units_tl, fwd_end = S.slide_streamed_timeline(st)
             tls.append((units_tl, fwd_end))
             per_step.append(dict(s=times[-1], **unit_spread(units_tl, sizes)))
+        # steps enqueued back to back (slide_model_step_streamed_async): each
+        # call returns once the step before has finished its updates, so the
+        # interval between returns is the steady-state step; the next step's
+        # forward sweep overlaps this step's last write-backs
+        pipe_returns = []
+        t_pipe0 = time.perf_counter()
+        for k in range(args.streamed_steps + 1):
+            pg.step = 100 + k
+            S.slide_model_step_streamed_async(st, fn_pool, pg, hp)
+            pipe_returns.append(time.perf_counter())
+        S.slide_streamed_sync(st)
+        t_pipe1 = time.perf_counter()
+        pipe_steps = [b - a for a, b in zip(pipe_returns[1:], pipe_returns[2:])]
         monitor_after = link_monitor(torch, arena=arena)
         if arena is not None:
             arena.reset(probe_mark)
@@ -829,6 +842,11 @@ def run_streamed(args, S, torch, synth, key, arena=None):
                          f"is extrapolated to the whole model's {N} parameters"}
     t_roof = link_roofline_s(link, N, in_hbm)
     per_dir = 12 * N if in_hbm else 14 * N
+    G = 1e9
+    # with steps overlapped, the forward sweep shares the link with the write-back
+    t_roof_pipe = max(per_dir / (link["h2d_concurrent_gbs"] * G), per_dir / (link["d2h_concurrent_gbs"] * G),
+                      2 * per_dir / (link["bidir_gbs"] * G))
+    s_pipe = statistics.median(pipe_steps) if pipe_steps else None
     return {"workload": w.name, "description": w.description, "params": N, "replicas": w.R,
             "steps": args.streamed_steps, "s_per_step": s_step, "s_per_step_each": times,
             "s_per_step_min": min(times), "s_per_step_mean": statistics.mean(times),
@@ -847,7 +865,14 @@ def run_streamed(args, S, torch, synth, key, arena=None):
             "cpu_baseline": cpu,
             "timeline_fastest_step": overlap_fast, "timeline_slowest_step": overlap_slow,
             "bf16_delivery": delivery,
-            "timing": "host wall clock around each synchronous model step; s_per_step is the median"}
+            "timing": "host wall clock around each synchronous model step; s_per_step is the median",
+            "pipelined": {"s_per_step": s_pipe, "roofline_s": t_roof_pipe,
+                          "frac": (t_roof_pipe / s_pipe) if s_pipe else None,
+                          "s_per_step_each": pipe_steps,
+                          "s_per_step_incl_last_drain": (t_pipe1 - t_pipe0) / (args.streamed_steps + 1),
+                          "roofline": "max(B/B'_h2d, B/B'_d2h, 2B/B_bidir), B the bytes each way per step",
+                          "timing": "intervals between the returns of slide_model_step_streamed_async calls "
+                                    "(each returns once the step before has finished its updates)"}}
 
 
 # --------------------------------------------------------------- ours ----
@@ -1167,6 +1192,9 @@ def compact_streamed(leg):
         out["pinned_arena"] = leg["pinned_arena"]
     if leg.get("cpu_baseline"):
         out["cpu_s_per_step"] = _r(leg["cpu_baseline"]["s_per_step_extrapolated"], 3)
+    pp = leg.get("pipelined")
+    if pp and pp.get("s_per_step"):
+        out["async_s_per_step"] = _r(pp["s_per_step"])
     return out
 
 

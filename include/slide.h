@@ -270,6 +270,40 @@ SLIDE_API slide_status slide_layer_step_host(slide_state *st, int32_t layer, con
 SLIDE_API slide_status slide_model_step_streamed(slide_state *st, slide_grad_fn fn, void *user,
                                        const slide_adam_hparams *hp);
 
+/* slide_model_step_streamed without the wait at its end: returns once the
+ * step is enqueued, so the next step's first copies (the forward sweep's BF16
+ * deliveries) run while this step's last write-backs drain.  Before enqueuing
+ * it waits (bounded) for the updates of an earlier asynchronous step, whose
+ * write-back may still be in flight; every unit's next delivery and copy-in
+ * waits on the device for that unit's own write-back, so the same-version and
+ * one-update-per-unit invariants hold as for the synchronous call.  grad_fn
+ * may therefore be called while the previous step still runs on the GPU (its
+ * work is ordered behind that step's on the stream it is given).  Unit
+ * versions advance when the step is enqueued.  slide_streamed_sync waits for
+ * the last step and reports its status; slide_layer_get, slide_layer_set,
+ * slide_deliver_bf16 and slide_streamed_timeline wait for it first.  A
+ * non-finite mean gradient (SLIDE_FLAG_CHECK_FINITE) seen by an asynchronous
+ * step is reported by the next slide_streamed_sync or synchronous step; a
+ * bounded wait that runs out is reported by the next call and marks the state
+ * aborted.
+ * Defined by: the passages of slide_model_step_streamed; the overlap across
+ * iterations is the layer-streaming pipeline of "An Efficient Heterogeneous
+ * Co-Design for Fine-Tuning on a Single GPU", section 2.1 (prefetch of the
+ * next layer while the current one is processed and the previous one is
+ * updated). */
+SLIDE_API slide_status slide_model_step_streamed_async(slide_state *st, slide_grad_fn fn, void *user,
+                                                       const slide_adam_hparams *hp);
+
+/* Wait (bounded) for the last slide_model_step_streamed_async of a streamed
+ * state and report the status of the asynchronous steps since the last
+ * report: SLIDE_ERR_TIMEOUT (a bounded wait ran out; the state is aborted),
+ * SLIDE_ERR_NONFINITE (with SLIDE_FLAG_CHECK_FINITE; the step was applied) or
+ * SLIDE_OK.  A no-op returning SLIDE_OK when nothing is pending.
+ * Defined by: the same passages as slide_model_step_streamed ("SlideDP:
+ * Scaling Host-Resident LLM Fine-Tuning Across Multiple GPUs", Method steps:
+ * a layer is delivered again only after its update is written back). */
+SLIDE_API slide_status slide_streamed_sync(slide_state *st);
+
 /* Copy host arrays into a layer's master / m / v (any may be NULL: left
  * unchanged) and set its step count t (>= 0).  Also rewrites the BF16 copy as
  * bf16(master) when master is given.  Synchronous.  Clears the aborted mark

@@ -84,6 +84,10 @@ def _load():
     L.slide_layer_step_host.argtypes = [P, C.c_int32, C.POINTER(C.c_void_p), C.POINTER(slide_adam_hparams), P, P]
     L.slide_layer_step_host.restype = S
     L.slide_model_step_streamed.argtypes = [P, P, P, C.POINTER(slide_adam_hparams)]
+    L.slide_model_step_streamed_async.argtypes = [P, P, P, C.POINTER(slide_adam_hparams)]
+    L.slide_model_step_streamed_async.restype = S
+    L.slide_streamed_sync.argtypes = [P]
+    L.slide_streamed_sync.restype = S
     L.slide_model_step_streamed.restype = S
     L.slide_layer_set.argtypes = [P, C.c_int32, P, P, P, C.c_int64]
     L.slide_layer_set.restype = S
@@ -256,6 +260,21 @@ def slide_model_step_streamed(st: SlideState, fn, user, hp: slide_adam_hparams) 
     else:
         user_ptr = C.cast(C.byref(user), C.c_void_p)
     _check(_lib().slide_model_step_streamed(C.c_void_p(st.handle), fn_ptr, user_ptr, C.byref(hp)))
+
+
+def slide_model_step_streamed_async(st: SlideState, fn, user, hp: slide_adam_hparams) -> None:
+    """slide_model_step_streamed returning once enqueued (see include/slide.h);
+    fn and user must stay alive until the step has been synced."""
+    fn_ptr = C.c_void_p(fn) if isinstance(fn, int) else C.cast(fn, C.c_void_p)
+    if user is None or isinstance(user, int):
+        user_ptr = C.c_void_p(user)
+    else:
+        user_ptr = C.cast(C.byref(user), C.c_void_p)
+    _check(_lib().slide_model_step_streamed_async(C.c_void_p(st.handle), fn_ptr, user_ptr, C.byref(hp)))
+
+
+def slide_streamed_sync(st: SlideState) -> None:
+    _check(_lib().slide_streamed_sync(C.c_void_p(st.handle)))
 
 
 def slide_layer_set(st: SlideState, layer: int, master=None, m=None, v=None, step: int = 0) -> None:

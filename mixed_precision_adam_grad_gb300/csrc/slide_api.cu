@@ -693,6 +693,8 @@ slide_status slide_layer_set(slide_state *st, int32_t layer, const float *master
     DeviceGuard guard(st->device);
     if (!guard.ok)
         return fail(SLIDE_ERR_CUDA, "cudaSetDevice failed");
+    if ((rc = engine_quiesce(st)) != SLIDE_OK)  // a step still in flight (slide_model_step_streamed_async)
+        return rc;
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess)
         return fail_cuda(e, "cudaDeviceSynchronize");
@@ -740,6 +742,8 @@ slide_status slide_layer_get(slide_state *st, int32_t layer, float *master, floa
     DeviceGuard guard(st->device);
     if (!guard.ok)
         return fail(SLIDE_ERR_CUDA, "cudaSetDevice failed");
+    if ((rc = engine_quiesce(st)) != SLIDE_OK)  // a step still in flight (slide_model_step_streamed_async)
+        return rc;
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess)
         return fail_cuda(e, "cudaDeviceSynchronize");
@@ -858,6 +862,8 @@ slide_status slide_deliver_bf16(slide_state *st, int32_t layer, void *const *dst
     DeviceGuard guard(st->device);
     if (!guard.ok)
         return fail(SLIDE_ERR_CUDA, "cudaSetDevice failed");
+    if ((rc = engine_quiesce(st)) != SLIDE_OK)  // the copy being delivered may still be in flight
+        return rc;
     cudaStream_t s = (cudaStream_t)stream;
     const size_t n = (size_t)L.n;
     cudaError_t e = cudaSuccess;
@@ -905,8 +911,8 @@ slide_status slide_streamed_timeline(slide_state *st, double *out, int64_t cap)
     return rc;
 }
 
-slide_status slide_model_step_streamed(slide_state *st, slide_grad_fn fn, void *user,
-                                       const slide_adam_hparams *hp)
+static slide_status model_step_streamed(slide_state *st, slide_grad_fn fn, void *user,
+                                        const slide_adam_hparams *hp, bool wait_for_end)
 {
     if (!st)
         return fail(SLIDE_ERR_INVALID_ARG, "state is NULL");
@@ -925,7 +931,34 @@ slide_status slide_model_step_streamed(slide_state *st, slide_grad_fn fn, void *
     DeviceGuard guard(st->device);
     if (!guard.ok)
         return fail(SLIDE_ERR_CUDA, "cudaSetDevice failed");
-    rc = engine_step(st, fn, user, *hp);
+    rc = engine_step(st, fn, user, *hp, wait_for_end);
+    if (rc == SLIDE_OK)
+        clear_error();
+    return rc;
+}
+
+slide_status slide_model_step_streamed(slide_state *st, slide_grad_fn fn, void *user,
+                                       const slide_adam_hparams *hp)
+{
+    return model_step_streamed(st, fn, user, hp, true);
+}
+
+slide_status slide_model_step_streamed_async(slide_state *st, slide_grad_fn fn, void *user,
+                                             const slide_adam_hparams *hp)
+{
+    return model_step_streamed(st, fn, user, hp, false);
+}
+
+slide_status slide_streamed_sync(slide_state *st)
+{
+    if (!st)
+        return fail(SLIDE_ERR_INVALID_ARG, "state is NULL");
+    if (st->cfg.residency != SLIDE_RESIDENCY_HOST_STREAMED || !st->engine)
+        return fail(SLIDE_ERR_STATE, "slide_streamed_sync needs the host-streamed residency");
+    DeviceGuard guard(st->device);
+    if (!guard.ok)
+        return fail(SLIDE_ERR_CUDA, "cudaSetDevice failed");
+    slide_status rc = engine_sync(st);
     if (rc == SLIDE_OK)
         clear_error();
     return rc;

@@ -101,7 +101,13 @@ inline size_t host_input_bytes(const slide_config &cfg, int64_t max_numel)
 slide_status engine_create(slide_state *st);
 void engine_destroy(slide_state *st);
 size_t engine_device_bytes(const slide_config &cfg, int64_t max_numel);
-slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const slide_adam_hparams &hp);
+slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const slide_adam_hparams &hp,
+                         bool wait_for_end);
+// Wait for a step enqueued by slide_model_step_streamed_async (no-op otherwise)
+// and report the status words of the steps since the last report.
+slide_status engine_sync(slide_state *st);
+// Wait for such a step without reading the status words.
+slide_status engine_quiesce(slide_state *st);
 slide_status engine_timeline(slide_state *st, double *out, int64_t cap);
 // A device buffer of the window (idle between steps) of *capacity bytes, for
 // moving data between caller memory and the pinned state by DMA only.

@@ -119,6 +119,11 @@ struct StreamEngine {
     cudaStream_t s_h2d = nullptr, s_comp = nullptr, s_d2h = nullptr;
     // per unit, timing events (also the timeline of the last step)
     std::vector<cudaEvent_t> h2d_begin, theta_done, h2d_done, kern_done, d2h_begin, d2h_end;
+    // per unit: its whole write-back (BF16 copy, master, m, v) has reached host
+    // memory; the next step's delivery and copy-in of the unit wait for it
+    std::vector<cudaEvent_t> wb_done;
+    bool pending = false;          // a step was enqueued without waiting for its end
+    bool nonfinite_seen = false;   // such a step saw a non-finite mean gradient (not yet reported)
     std::vector<char> recorded;  // unit reached its write-back in the last step
     // host clock (ms since the step's first event was enqueued) at which the
     // copy-in of unit l, and its update and write-back, were fully enqueued
@@ -175,6 +180,7 @@ static void destroy_engine_objects(StreamEngine *E)
     }
     for (auto *v : {&E->h2d_begin, &E->theta_done, &E->h2d_done, &E->kern_done, &E->d2h_begin, &E->d2h_end})
         kill(*v);
+    kill(E->wb_done);
     for (cudaEvent_t ev : {E->step_start, E->fwd_done, E->sweep_done[0], E->sweep_done[1], E->sweep_done[2]})
         if (ev)
             cudaEventDestroy(ev);
@@ -246,6 +252,10 @@ slide_status engine_create(slide_state *st)
             if (e == cudaSuccess)
                 e = cudaEventCreate(&ev);
     }
+    E->wb_done.assign(L, nullptr);
+    for (auto &ev : E->wb_done)
+        if (e == cudaSuccess)
+            e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
     E->recorded.assign(L, 0);
     E->host_copyin_enqueued.assign(L, __builtin_nan(""));
     E->host_unit_enqueued.assign(L, __builtin_nan(""));
@@ -325,9 +335,85 @@ static slide_status wait_event(cudaEvent_t ev, uint32_t timeout_ms, const char *
     }
 }
 
-slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const slide_adam_hparams &hp)
+// Read and clear the slots' status words (their kernels must be done):
+// bit 1, a pipeline wait in the update kernel ran out; bit 0, a non-finite
+// mean gradient (with SLIDE_FLAG_CHECK_FINITE).
+static unsigned take_slot_word(slide_state *st)
 {
     StreamEngine *E = st->engine;
+    unsigned word = 0;
+    for (int k = 0; k < kSlots; ++k) {
+        unsigned w = 0;
+        if (cudaMemcpy(&w, E->slots[k].scratch.status, sizeof w, cudaMemcpyDeviceToHost) == cudaSuccess && w)
+            cudaMemset(E->slots[k].scratch.status, 0, sizeof w);
+        word |= w;
+    }
+    return word;
+}
+
+// Wait (bounded) for a step enqueued without waiting for its end: its
+// update work only (the write-back may still drain), or everything.
+static slide_status wait_pending(slide_state *st, bool everything)
+{
+    StreamEngine *E = st->engine;
+    if (!E || !E->pending)
+        return SLIDE_OK;
+    const int last = everything ? 3 : 2;  // sweep_done: H2D, compute, D2H
+    for (int k = 0; k < last; ++k) {
+        slide_status rc = wait_event(E->sweep_done[k], st->cfg.timeout_ms, "streamed step (pipelined)");
+        if (rc != SLIDE_OK) {
+            st->aborted = true;
+            return rc;
+        }
+    }
+    if (everything)
+        E->pending = false;
+    return SLIDE_OK;
+}
+
+slide_status engine_quiesce(slide_state *st)
+{
+    return st->engine ? wait_pending(st, true) : SLIDE_OK;
+}
+
+slide_status engine_sync(slide_state *st)
+{
+    StreamEngine *E = st->engine;
+    if (!E)
+        return SLIDE_OK;
+    slide_status rc = wait_pending(st, true);
+    if (rc != SLIDE_OK)
+        return rc;
+    const unsigned word = take_slot_word(st);
+    if (word & 2u) {
+        st->aborted = true;
+        return fail(SLIDE_ERR_TIMEOUT, "a pipeline wait inside the update kernel reached its limit");
+    }
+    const bool nonfinite = (word & 1u) || E->nonfinite_seen;
+    E->nonfinite_seen = false;
+    if (nonfinite && (st->cfg.flags & SLIDE_FLAG_CHECK_FINITE))
+        return fail(SLIDE_ERR_NONFINITE, "a non-finite mean gradient was seen (the step was applied)");
+    return SLIDE_OK;
+}
+
+slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const slide_adam_hparams &hp,
+                         bool wait_for_end)
+{
+    StreamEngine *E = st->engine;
+    if (E->pending) {
+        // the step before was enqueued without waiting: let its updates finish
+        // (its write-back may keep draining behind this step's first copies)
+        slide_status prc = wait_pending(st, false);
+        if (prc != SLIDE_OK)
+            return prc;
+        const unsigned word = take_slot_word(st);
+        if (word & 2u) {
+            st->aborted = true;
+            return fail(SLIDE_ERR_TIMEOUT, "a pipeline wait inside the update kernel reached its limit");
+        }
+        if (word & 1u)
+            E->nonfinite_seen = true;  // reported at the next sync or synchronous step
+    }
     const int L = (int)st->layers.size();
     const int R = st->cfg.n_replicas;
     const int64_t t = st->layers[0].t + 1;
@@ -362,6 +448,8 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
     for (int l = 0; l < L && w_slot && e == cudaSuccess; ++l) {
         Slot &s = E->slots[l % kSlots];
         const LayerState &U = st->layers[l];
+        // the host mirror of l holds the previous step's copy once its write-back is done
+        e = cudaStreamWaitEvent(E->s_h2d, E->wb_done[l], 0);
         for (int k = 0; k < E->n_chunks(U.n) && e == cudaSuccess; ++k) {
             const Chunk c = E->chunk(U.n, k);
             e = E->wait_freed(E->s_h2d, s, kW, c);
@@ -382,7 +470,11 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
         Slot &s = E->slots[l % kSlots];
         const LayerState &U = st->layers[l];
         const int K = E->n_chunks(U.n);
-        cudaError_t err = cudaEventRecord(E->h2d_begin[l], E->s_h2d);
+        // the host master, m and v of l hold the previous step's values once
+        // its write-back is done
+        cudaError_t err = cudaStreamWaitEvent(E->s_h2d, E->wb_done[l], 0);
+        if (err == cudaSuccess)
+            err = cudaEventRecord(E->h2d_begin[l], E->s_h2d);
         if (!w_slot) {
             for (int k = 0; k < K && err == cudaSuccess; ++k) {
                 const Chunk c = E->chunk(U.n, k);
@@ -529,6 +621,8 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
         }
         if (e == cudaSuccess)
             e = cudaEventRecord(E->d2h_end[l], E->s_d2h);
+        if (e == cudaSuccess)
+            e = cudaEventRecord(E->wb_done[l], E->s_d2h);
         if (e == cudaSuccess) {
             E->recorded[l] = 1;
             E->host_unit_enqueued[l] = host_ms();
@@ -537,6 +631,20 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
     }
     if (e != cudaSuccess && rc == SLIDE_OK)
         rc = fail_cuda(e, "streamed step: enqueue");
+
+    if (!wait_for_end && rc == SLIDE_OK) {
+        // return once enqueued: the next step (or a sync) waits for this one
+        const cudaStream_t ss[3] = {E->s_h2d, E->s_comp, E->s_d2h};
+        for (int k = 0; k < 3 && e == cudaSuccess; ++k)
+            e = cudaEventRecord(E->sweep_done[k], ss[k]);
+        if (e == cudaSuccess) {
+            E->pending = true;
+            for (LayerState &U : st->layers)
+                U.t = t;
+            return SLIDE_OK;
+        }
+        rc = fail_cuda(e, "streamed step: record");
+    }
 
     // bounded host waits for everything enqueued on the three streams
     slide_status wrc = SLIDE_OK;
@@ -560,10 +668,13 @@ slide_status engine_step(slide_state *st, slide_grad_fn fn, void *user, const sl
     if (rc == SLIDE_OK && wrc != SLIDE_OK)
         rc = wrc;
 
+    E->pending = false;
     if (rc == SLIDE_OK) {
         for (LayerState &U : st->layers)
             U.t = t;
-        if (check && (word & 1u))
+        const bool nonfinite = (word & 1u) || E->nonfinite_seen;
+        E->nonfinite_seen = false;
+        if (check && nonfinite)
             return fail(SLIDE_ERR_NONFINITE, "a non-finite mean gradient was seen (the step was applied)");
         return SLIDE_OK;
     }
@@ -590,6 +701,11 @@ slide_status engine_timeline(slide_state *st, double *out, int64_t cap)
     constexpr int kPer = 8;
     if (cap < kPer * (int64_t)L + 1)
         return fail(SLIDE_ERR_INVALID_ARG, "timeline buffer needs 8 * n_layers + 1 doubles");
+    if (E->pending) {
+        slide_status rc = engine_quiesce(st);
+        if (rc != SLIDE_OK)
+            return rc;
+    }
     const double nan = __builtin_nan("");
     auto since = [&](cudaEvent_t ev) -> double {
         float ms = 0.0f;

@@ -129,7 +129,9 @@ def _full_record():
                 "cpu_baseline": {"value": 0.05, "unit": "Gparam/s", "cores": 1, "kind": "oracle",
                                  "s_per_step_extrapolated": 140.0, "sample": "s" * 300},
                 "timeline_fastest_step": {"units_ms": units}, "timeline_slowest_step": {"units_ms": units},
-                "bf16_delivery": {"full": {"ms": 66.4}}, "timing": "t"}
+                "bf16_delivery": {"full": {"ms": 66.4}}, "timing": "t",
+                "pipelined": {"s_per_step": 0.59, "roofline_s": 0.578, "frac": 0.98,
+                              "s_per_step_each": [0.59] * 5, "s_per_step_incl_last_drain": 0.6}}
     hbm = {"workload": "h2560_R4_clip", "description": "d", "params": 100_930_560, "replicas": 4, "steps": 20,
            "value": 155.0, "unit": "Gparam/s", "ms_per_step": 0.65, "hbm_gbs": 6500.0,
            "roofline": {"bound": "hbm", "kernel": "grad_reduce_adamw_cast", "achieved": 6700.0, "peak": 6779.0,
@@ -205,6 +207,7 @@ def test_compact_headline_is_last_and_small(capsys, tmp_path):
     assert h["e2e"]["h2d_bytes_per_step"] == 16 * 330_311_680
     st = h["streamed"]
     assert st["h8192x8_streamed"]["frac"] == 0.97 and st["h8192x8_streamed"]["unit_max_over_median"] == 1.1
+    assert st["h8192x8_streamed"]["async_s_per_step"] == 0.59
     assert "skipped" in st["h8192x8_streamed+x"]
     assert st["h5120x40_streamed"]["bf16_in_hbm"] is True
     assert len(h["chunk_sweep"]["h5120x40_streamed"]["points"]) == 8

@@ -158,6 +158,60 @@ def test_streamed_toy_every_element(S, clip, chunk, chunk_d2h, fp32, in_hbm, are
         S.slide_state_destroy(st)
 
 
+@pytest.mark.parametrize("in_hbm,chunk,chunk_d2h", [(False, 64 << 10, 0), (True, 4096, 64 << 10),
+                                                   (False, 768, 1 << 20), (True, 1 << 20, 256)])
+def test_streamed_async_steps_every_element(S, in_hbm, chunk, chunk_d2h):
+    """Steps enqueued with slide_model_step_streamed_async back to back (each
+    unit's next delivery and copy-in wait on the device for its own previous
+    write-back), then mixed with a synchronous step and with accessors that
+    must wait for a step in flight: every element against the oracle."""
+    w = toy(clip=0.5)
+    w.steps = 5
+    flags = S.SLIDE_FLAG_BF16_COPY_IN_HBM if in_hbm else 0
+    sizes = [u.numel for u in w.units]
+    st = S.slide_state_create(sizes, w.R, residency=S.SLIDE_RESIDENCY_HOST_STREAMED, chunk_bytes=chunk,
+                              chunk_bytes_d2h=chunk_d2h, flags=flags)
+    try:
+        init_streamed(S, w, st)
+        ref = [[synth.master(u.numel, w.seed, unit=ui), np.zeros(u.numel, np.float32),
+                np.zeros(u.numel, np.float32), np.zeros(u.numel, np.uint16)] for ui, u in enumerate(w.units)]
+        hp = S.hparams(*w.hparams_tuple())
+
+        def compare(t):
+            for ui, u in enumerate(w.units):
+                a, b, c = (np.empty(u.numel, np.float32) for _ in range(3))
+                wb = np.empty(u.numel, np.uint16)
+                assert S.slide_layer_get(st, ui, a, b, c, wb) == t
+                pu.assert_parity([pu.compare_fp32("theta", a, ref[ui][0]), pu.compare_fp32("m", b, ref[ui][1]),
+                                  pu.compare_fp32("v", c, ref[ui][2]), pu.compare_bf16("w", wb, ref[ui][3])])
+
+        def oracle_to(t0, t1):
+            for t in range(t0, t1 + 1):
+                for ui, u in enumerate(w.units):
+                    oracle.layer_step([pu.unit_grad_host(w, ui, t, r) for r in range(w.R)], *ref[ui],
+                                      pu.hp_oracle(w), t)
+
+        # three asynchronous steps back to back, then a sync
+        for t in (1, 2, 3):
+            S.slide_model_step_streamed_async(st, synth.grad_fn_address(), ModelGradsHolder(w, t).mg, hp)
+        S.slide_streamed_sync(st)
+        oracle_to(1, 3)
+        compare(3)
+        # an asynchronous step read back without a sync (the accessor waits),
+        # then a synchronous step behind another asynchronous one
+        S.slide_model_step_streamed_async(st, synth.grad_fn_address(), ModelGradsHolder(w, 4).mg, hp)
+        oracle_to(4, 4)
+        compare(4)
+        S.slide_model_step_streamed_async(st, synth.grad_fn_address(), ModelGradsHolder(w, 5).mg, hp)
+        S.slide_model_step_streamed(st, synth.grad_fn_address(), ModelGradsHolder(w, 6).mg, hp)
+        oracle_to(5, 6)
+        compare(6)
+        check_timeline(S, st, sizes)
+        S.slide_streamed_sync(st)   # nothing pending: a no-op
+    finally:
+        S.slide_state_destroy(st)
+
+
 @pytest.mark.parametrize("sizes,in_hbm", [([123_457], False), ([123_457], True), ([0, 70_001], False),
                                            ([70_001, 0], True), ([5, 3], False)])
 def test_streamed_few_units_every_element(S, sizes, in_hbm):
