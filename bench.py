@@ -316,6 +316,18 @@ def measure_hbm_workload(args, S, torch, synth, peak, w, max_steps=500):
         ms = start.elapsed_time(stop)
         upd = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
         pre = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+        ms_serialised = None
+        if clip:
+            # The steps above carry trace events between pre-pass and update,
+            # which serialise them; the step as a caller runs it (the update
+            # launched behind the pre-pass, overlapping its end) is timed here.
+            ms_serialised = ms
+            start.record(stream)
+            for k in range(K):
+                S.slide_layer_step(st, 0, batches[k % 2], hp, stream)
+            stop.record(stream)
+            torch.cuda.synchronize()
+            ms = start.elapsed_time(stop)
     finally:
         S.slide_state_destroy(st)
     b_upd, b_pre = (26 + gsize * R) * n, (gsize * R * n if clip else 0)
@@ -329,7 +341,9 @@ def measure_hbm_workload(args, S, torch, synth, peak, w, max_steps=500):
                          "bytes_per_param": 26 + gsize * R, "avg_launch_ms": upd, "launches": K},
             "prepass": ({"achieved": b_pre / (pre * 1e-3) / 1e9, "frac": b_pre / (pre * 1e-3) / 1e9 / peak,
                          "avg_launch_ms": pre, "bytes_per_param": gsize * R} if clip else None),
-            "step_roofline_frac": (b_upd + b_pre) / (ms / K * 1e-3) / 1e9 / peak}
+            "step_roofline_frac": (b_upd + b_pre) / (ms / K * 1e-3) / 1e9 / peak,
+            "serialised_step_frac": ((b_upd + b_pre) / (ms_serialised / K * 1e-3) / 1e9 / peak
+                                     if clip else None)}
 
 
 # ----------------------------------------------------------- streamed ----
@@ -971,7 +985,8 @@ def run_ours(args):
         torch.cuda.synchronize()
         start.record(stream)
         for k in range(K):
-            S.slide_trace_events(st, ev[k][0], ev[k][1], ev[k][2])
+            if not clip:   # with the clip, an event between pre-pass and update would serialise them
+                S.slide_trace_events(st, ev[k][0], ev[k][1], ev[k][2])
             step(k)
         stop.record(stream)
         torch.cuda.synchronize()
@@ -980,6 +995,19 @@ def run_ours(args):
         clocks = sampler.stop()
         S.slide_trace_events(st)
         ms_total = start.elapsed_time(stop)
+        serialised_ms = None
+        if clip:
+            # The kernel split: K more steps, each with its trace events, which
+            # make the update wait for the pre-pass's end.
+            s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s0.record(stream)
+            for k in range(K):
+                S.slide_trace_events(st, ev[k][0], ev[k][1], ev[k][2])
+                step(K + k)
+            s1.record(stream)
+            torch.cuda.synchronize()
+            S.slide_trace_events(st)
+            serialised_ms = s0.elapsed_time(s1) / K
         pre_ms = [e[0].elapsed_time(e[1]) for e in ev]
         upd_ms = [e[1].elapsed_time(e[2]) for e in ev]
         ms_total = max_over_ranks(ms_total, dist)
@@ -1123,7 +1151,11 @@ def run_ours(args):
                      "bytes_per_launch": bytes_upd, "avg_launch_ms": upd_avg,
                      "bytes_per_param": 26 + 2 * R, "launches": K},
         "prepass": ({"kernel": "grad_sqnorm_pipe", "achieved": ach_pre, "unit": "GB/s", "frac": ach_pre / peak,
-                     "bytes_per_launch": bytes_pre, "avg_launch_ms": pre_avg} if clip else None),
+                     "bytes_per_launch": bytes_pre, "avg_launch_ms": pre_avg,
+                     "split_note": "pre-pass and update timed in K further steps with trace events between "
+                                   "them, which serialise them; the timed region runs the steps without them",
+                     "serialised_step_frac": step_bytes / (serialised_ms * 1e-3) / 1e9 / peak}
+                    if clip else None),
         "step_roofline_frac": (step_bytes / (ms_step * 1e-3) / 1e9) / peak,
         "gpu_launches": K * (2 if clip else 1),
         "clocks": clocks,
@@ -1166,6 +1198,8 @@ def compact_hbm_leg(leg):
            "step_frac": _r(leg["step_roofline_frac"]), "launches": leg["steps"]}
     if leg.get("prepass"):
         out["prepass_frac"] = _r(leg["prepass"]["frac"])
+    if leg.get("serialised_step_frac") is not None:
+        out["serialised_step_frac"] = _r(leg["serialised_step_frac"])
     return out
 
 
@@ -1188,8 +1222,9 @@ def compact_streamed(leg):
            "unit_max_over_median": _r(statistics.median(spreads), 3) if spreads else None,
            "unit_max_over_median_worst": _r(spreads[-1], 3) if spreads else None,
            "chunk_mib": [leg.get("chunk_h2d_mib", leg.get("chunk_mib")), leg.get("chunk_d2h_mib", leg.get("chunk_mib"))]}
-    if "pinned_arena" in leg:
-        out["pinned_arena"] = leg["pinned_arena"]
+    if "pinned_arena" in leg:   # "shared": the run's one pinned arena; else how the state pinned its own
+        a = leg["pinned_arena"]
+        out["arena"] = "shared" if a.startswith("the run's") else a
     if leg.get("cpu_baseline"):
         out["cpu_s_per_step"] = _r(leg["cpu_baseline"]["s_per_step_extrapolated"], 3)
     pp = leg.get("pipelined")
@@ -1221,7 +1256,7 @@ def compact_headline(full):
     line["hbm_gbs"] = _r(full["hbm_gbs"])
     line["step_roofline_frac"] = _r(full["step_roofline_frac"])
     if full.get("prepass"):
-        line["prepass"] = _pick(full["prepass"], ("kernel", "achieved", "frac", "avg_launch_ms"))
+        line["prepass"] = _pick(full["prepass"], ("kernel", "achieved", "frac", "avg_launch_ms", "serialised_step_frac"))
     line["gpu_launches"] = full["gpu_launches"]
     ck = full.get("clocks") or {}
     line["clocks"] = {"sm_mhz": ck.get("sm_mhz"), "sm_max_mhz": ck.get("sm_max_mhz"),

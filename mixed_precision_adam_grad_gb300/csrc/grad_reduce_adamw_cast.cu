@@ -38,6 +38,16 @@
 // 2R bytes per parameter) that writes one double-precision partial per block;
 // the fused kernel turns the partials into the coefficient in its prologue,
 // in the same fixed order in every block, so every block uses the same bits.
+// Two things make the pair cost less than two passes back to back:
+//  - the clipped step is launched behind the pre-pass with programmatic
+//    serialisation (where a CTA of each fits on an SM together): its CTAs
+//    start while the pre-pass runs, fill their rings with gradients and
+//    FP32 state, and wait for the pre-pass's end only before reading the
+//    partials, so no launch gap and no pipeline ramp sit between the two;
+//  - the clipped step walks its tiles from the last to the first, so it
+//    begins on the gradients the pre-pass read last, which L2 still holds.
+// Measured on a 101M-parameter layer with four replicas, the whole clipped
+// step went from 0.973 to 0.984 of the copy peak at 42 bytes per parameter.
 //
 // Every wait on an mbarrier is bounded (kWaitLimitNs of wall time); a wait
 // that runs out sets bit 1 of the status word, waits (bounded) for the bulk
@@ -312,6 +322,34 @@ __device__ __forceinline__ void bulk_load(void *dst_smem, const void *src_gmem, 
         : "memory");
 }
 
+// The same copy with an L2 eviction-priority policy (from make_evict_first).
+__device__ __forceinline__ void bulk_load_hint(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar,
+                                               uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
+        "%4;" ::"r"(smem_addr(dst_smem)),
+        "l"(src_gmem), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// An L2 policy that marks the lines a load brings in (or hits) as the first to
+// evict: for data read once.
+__device__ __forceinline__ uint64_t make_evict_first()
+{
+    uint64_t policy;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
+    return policy;
+}
+
+// Programmatic dependent launch.  launch_dependents lets the next kernel of
+// the stream, when launched with programmatic serialisation, start before this
+// one ends; wait_prerequisites blocks until the kernel this one was launched
+// behind has ended and its writes are visible (it returns at once for a plain
+// launch).
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 template <typename G, int R>
 struct Pipe {
     static constexpr uint32_t kGradBytes = kTile * sizeof(G);
@@ -325,10 +363,17 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_grad_reduce_adamw_cast(KArg
 {
     using P = Pipe<G, R>;
     using V4 = typename GradT<G>::V4;
+    // Loads marked evict-first in L2, for the one instance where that was
+    // measured faster: one BF16 replica, no clip (0.980 against 0.976 of the
+    // copy peak on a 101M-parameter layer).  With R = 8 it was slower (0.981
+    // against 0.987), and with the clip it takes L2 from the gradients the
+    // pre-pass left there.
+    constexpr bool kHintL2 = R == 1 && !CLIP;
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * P::kStageBytes);
     uint64_t *empty = full + kStages;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t ntiles = a.n / kTile;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -337,45 +382,71 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_grad_reduce_adamw_cast(KArg
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    __syncthreads();
+
+    // Producer state.  The block's k-th tile is j = blockIdx.x + k * gridDim.x;
+    // with the clip it is processed as tile ntiles - 1 - j, so the step starts
+    // on the last tiles, whose gradients the clip pre-pass read last and L2
+    // still holds.
+    int p_stage = 0;
+    uint32_t p_phase = 0;
+    uint32_t issued = 0, issued_phase = 0;  // per stage: filled at least once, and that fill's parity
+    int64_t p_j = blockIdx.x;
+    const bool producer = warp == kConsumerWarps && lane == 0 && !a.test_stall;
+    const uint64_t policy = kHintL2 ? make_evict_first() : 0;
+    auto load = [&](void *dst, const void *src, uint32_t bytes) {
+        if constexpr (kHintL2)
+            bulk_load_hint(dst, src, bytes, &full[p_stage], policy);
+        else
+            bulk_load(dst, src, bytes, &full[p_stage]);
+    };
+    auto issue = [&]() {
+        const int64_t tile = CLIP ? ntiles - 1 - p_j : p_j;
+        unsigned char *base = smem + p_stage * P::kStageBytes;
+        mbar_arrive_expect_tx(&full[p_stage], P::kStageBytes);
+        const int64_t e0 = tile * kTile;
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            load(base + r * P::kGradBytes, static_cast<const G *>(a.g.p[r]) + e0, P::kGradBytes);
+        load(base + R * P::kGradBytes, a.theta + e0, P::kF32Bytes);
+        load(base + R * P::kGradBytes + P::kF32Bytes, a.m + e0, P::kF32Bytes);
+        load(base + R * P::kGradBytes + 2 * P::kF32Bytes, a.v + e0, P::kF32Bytes);
+        issued |= 1u << p_stage;
+        issued_phase = (issued_phase & ~(1u << p_stage)) | (p_phase << p_stage);
+        if (++p_stage == kStages) {
+            p_stage = 0;
+            p_phase ^= 1u;
+        }
+        p_j += gridDim.x;
+    };
+
     float coef = 1.0f;
     if constexpr (CLIP) {
+        // This kernel may be launched behind the clip pre-pass with
+        // programmatic serialisation, so it can start while the pre-pass
+        // runs.  Nothing the pre-pass writes is read before the wait: the
+        // ring's first fills read gradients and the FP32 state only (empty
+        // stages need no wait), the partials come after it.
+        if (producer)
+            for (int k = 0; k < kStages && p_j < ntiles; ++k)
+                issue();
+        wait_prerequisites();
         coef = clip_coef_from_partials(a.partials, a.n_partials, a.max_norm);  // includes __syncthreads
         if (blockIdx.x == 0 && threadIdx.x == 0 && a.coef_out)
             *a.coef_out = coef;
-    } else {
-        __syncthreads();
     }
-    const int64_t ntiles = a.n / kTile;
 
     if (warp == kConsumerWarps) {
         // ---- producer: one thread issues the bulk copies of each tile ----
-        if (lane != 0 || a.test_stall)
+        if (!producer)
             return;
-        int stage = 0;
-        uint32_t phase = 0;
-        uint32_t issued = 0, issued_phase = 0;  // per stage: filled at least once, and that fill's parity
         bool ok = true;
-        for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-            if (!mbar_wait(&empty[stage], phase ^ 1u)) {
+        while (p_j < ntiles) {
+            if (!mbar_wait(&empty[p_stage], p_phase ^ 1u)) {
                 ok = false;
                 break;
             }
-            unsigned char *base = smem + stage * P::kStageBytes;
-            mbar_arrive_expect_tx(&full[stage], P::kStageBytes);
-            const int64_t e0 = tile * kTile;
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-                bulk_load(base + r * P::kGradBytes, static_cast<const G *>(a.g.p[r]) + e0, P::kGradBytes,
-                          &full[stage]);
-            bulk_load(base + R * P::kGradBytes, a.theta + e0, P::kF32Bytes, &full[stage]);
-            bulk_load(base + R * P::kGradBytes + P::kF32Bytes, a.m + e0, P::kF32Bytes, &full[stage]);
-            bulk_load(base + R * P::kGradBytes + 2 * P::kF32Bytes, a.v + e0, P::kF32Bytes, &full[stage]);
-            issued |= 1u << stage;
-            issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-            if (++stage == kStages) {
-                stage = 0;
-                phase ^= 1u;
-            }
+            issue();
         }
         // No copy may still be landing in shared memory when the block ends:
         // wait (bounded) for the last fill of every stage.
@@ -393,7 +464,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_grad_reduce_adamw_cast(KArg
     bool bad = false;
     int stage = 0;
     uint32_t phase = 0;
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    for (int64_t j = blockIdx.x; j < ntiles; j += gridDim.x) {
+        const int64_t tile = CLIP ? ntiles - 1 - j : j;
         if (!mbar_wait(&full[stage], phase)) {
             if (a.status)
                 atomicOr(a.status, kStatusWaitLimit);
@@ -561,6 +633,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1) k_grad_sqnorm_pipe(SqArgs a)
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + P::kStages * P::kStageBytes);
     uint64_t *empty = full + P::kStages;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // The clipped step that follows may start now: it reads these partials
+    // only after this grid has ended.
+    launch_dependents();
     if (threadIdx.x == 0) {
         for (int i = 0; i < P::kStages; ++i) {
             mbar_init(&full[i], 1);
@@ -700,6 +775,27 @@ int sm_count(int device)
 
 
 
+// Whether a CTA of the clipped step fits on an SM beside a CTA of the clip
+// pre-pass (dynamic shared memory of each, plus a margin for their static
+// shared memory and the per-CTA reservation).  Only then is the step launched
+// to overlap the pre-pass: a step whose CTAs cannot sit beside the pre-pass's
+// would take the SMs the pre-pass leaves first, two CTAs to an SM, and run
+// unevenly.
+bool fits_beside_prepass(int device, uint32_t step_smem, uint32_t prepass_smem)
+{
+    static std::atomic<int> cache[kMaxDevices];
+    int per_sm = 0;
+    if (device >= 0 && device < kMaxDevices)
+        per_sm = cache[device].load(std::memory_order_relaxed);
+    if (per_sm == 0) {
+        if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device) != cudaSuccess)
+            return false;
+        if (device >= 0 && device < kMaxDevices)
+            cache[device].store(per_sm, std::memory_order_relaxed);
+    }
+    return (int64_t)step_smem + prepass_smem + 4096 <= per_sm;
+}
+
 // Raise the fused kernel's dynamic shared-memory limit on `device` (once per
 // device; the device must be current).  Setting the attribute also loads the
 // kernel's code on a lazily loading context.
@@ -712,6 +808,11 @@ cudaError_t prepare_pipeline_kernel(int device)
     if (device >= 0 && device < kMaxDevices && attr_set[device].load(std::memory_order_acquire))
         return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // The clipped step starts while the pre-pass still runs (one CTA of each
+    // per SM, 81-131 KB of shared memory each): ask for the largest shared
+    // memory carve-out so that both fit on an SM at once.
+    if (e == cudaSuccess && CLIP)
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess)
         return e;
     if (device >= 0 && device < kMaxDevices)
@@ -720,7 +821,7 @@ cudaError_t prepare_pipeline_kernel(int device)
 }
 
 template <typename G, int R, bool CLIP, bool CHECK>
-cudaError_t launch_step_r(const KArgs &a, int device, cudaStream_t stream)
+cudaError_t launch_step_r(const KArgs &a, int device, cudaStream_t stream, bool behind_prepass)
 {
     constexpr auto kern = k_grad_reduce_adamw_cast<G, R, CLIP, CHECK>;
     constexpr uint32_t smem = Pipe<G, R>::kSmemBytes;
@@ -733,32 +834,48 @@ cudaError_t launch_step_r(const KArgs &a, int device, cudaStream_t stream)
     const int64_t ntiles = a.n / kTile;
     if (grid > ntiles)
         grid = ntiles > 0 ? ntiles : 1;
+    if (CLIP && behind_prepass && fits_beside_prepass(device, smem, SqPipe<G, R>::kSmemBytes)) {
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(kPipeThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kern, a);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
     kern<<<(unsigned)grid, kPipeThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
 template <typename G, int R>
-cudaError_t launch_step_flags(const KArgs &a, bool clip, bool check, int device, cudaStream_t stream)
+cudaError_t launch_step_flags(const KArgs &a, bool clip, bool check, int device, cudaStream_t stream,
+                              bool behind_prepass)
 {
     if (clip)
-        return check ? launch_step_r<G, R, true, true>(a, device, stream)
-                     : launch_step_r<G, R, true, false>(a, device, stream);
-    return check ? launch_step_r<G, R, false, true>(a, device, stream)
-                 : launch_step_r<G, R, false, false>(a, device, stream);
+        return check ? launch_step_r<G, R, true, true>(a, device, stream, behind_prepass)
+                     : launch_step_r<G, R, true, false>(a, device, stream, behind_prepass);
+    return check ? launch_step_r<G, R, false, true>(a, device, stream, false)
+                 : launch_step_r<G, R, false, false>(a, device, stream, false);
 }
 
 template <typename G>
-cudaError_t launch_step_g(const KArgs &a, int R, bool clip, bool check, int device, cudaStream_t stream)
+cudaError_t launch_step_g(const KArgs &a, int R, bool clip, bool check, int device, cudaStream_t stream,
+                          bool behind_prepass)
 {
     switch (R) {
-    case 1: return launch_step_flags<G, 1>(a, clip, check, device, stream);
-    case 2: return launch_step_flags<G, 2>(a, clip, check, device, stream);
-    case 3: return launch_step_flags<G, 3>(a, clip, check, device, stream);
-    case 4: return launch_step_flags<G, 4>(a, clip, check, device, stream);
-    case 5: return launch_step_flags<G, 5>(a, clip, check, device, stream);
-    case 6: return launch_step_flags<G, 6>(a, clip, check, device, stream);
-    case 7: return launch_step_flags<G, 7>(a, clip, check, device, stream);
-    case 8: return launch_step_flags<G, 8>(a, clip, check, device, stream);
+    case 1: return launch_step_flags<G, 1>(a, clip, check, device, stream, behind_prepass);
+    case 2: return launch_step_flags<G, 2>(a, clip, check, device, stream, behind_prepass);
+    case 3: return launch_step_flags<G, 3>(a, clip, check, device, stream, behind_prepass);
+    case 4: return launch_step_flags<G, 4>(a, clip, check, device, stream, behind_prepass);
+    case 5: return launch_step_flags<G, 5>(a, clip, check, device, stream, behind_prepass);
+    case 6: return launch_step_flags<G, 6>(a, clip, check, device, stream, behind_prepass);
+    case 7: return launch_step_flags<G, 7>(a, clip, check, device, stream, behind_prepass);
+    case 8: return launch_step_flags<G, 8>(a, clip, check, device, stream, behind_prepass);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -773,6 +890,9 @@ cudaError_t prepare_sq_pipe(int device)
         return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(k_grad_sqnorm_pipe<G, R>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)SqPipe<G, R>::kSmemBytes);
+    if (e == cudaSuccess)  // room for the clipped step's CTA beside it (see prepare_pipeline_kernel)
+        e = cudaFuncSetAttribute(k_grad_sqnorm_pipe<G, R>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess)
         return e;
     if (device >= 0 && device < kMaxDevices)
@@ -900,7 +1020,7 @@ cudaError_t launch_grad_reduce_adamw_cast(const ReplicaPtrs &g, int R, int64_t n
                                           float *m, float *v, uint16_t *w, const AdamScalars &s,
                                           const ClipScratch *clip, int n_partials, float max_norm,
                                           bool check_finite, int device, cudaStream_t stream, bool test_stall,
-                                          bool f32_grads)
+                                          bool f32_grads, bool behind_prepass)
 {
     const bool do_clip = clip != nullptr && clip->partials != nullptr && max_norm > 0.0f;
     KArgs a{};
@@ -917,8 +1037,8 @@ cudaError_t launch_grad_reduce_adamw_cast(const ReplicaPtrs &g, int R, int64_t n
     a.coef_out = do_clip ? clip->coef : nullptr;
     a.status = clip ? clip->status : nullptr;
     a.test_stall = test_stall ? 1 : 0;
-    return f32_grads ? launch_step_g<float>(a, R, do_clip, check_finite, device, stream)
-                     : launch_step_g<uint16_t>(a, R, do_clip, check_finite, device, stream);
+    return f32_grads ? launch_step_g<float>(a, R, do_clip, check_finite, device, stream, behind_prepass)
+                     : launch_step_g<uint16_t>(a, R, do_clip, check_finite, device, stream, behind_prepass);
 }
 
 }  // namespace slide

@@ -530,11 +530,14 @@ static slide_status enqueue_layer_step(slide_state *st, LayerState &L, const Rep
             if (e != cudaSuccess)
                 return fail_cuda(e, "grad_sqnorm launch");
         }
+        // With the clip, the update is launched right behind the pre-pass
+        // and overlaps its end, unless a trace event has to separate them.
         if (st->trace[1])
             cudaEventRecord(st->trace[1], s);
         e = launch_grad_reduce_adamw_cast(g, R, L.n, L.theta, L.m, L.v, w, sc, &L.scratch, n_partials,
                                           clip ? hp->max_grad_norm : 0.0f, check, st->device, s,
-                                          (st->cfg.flags & SLIDE_FLAG_TEST_PIPELINE_STALL) != 0, f32g);
+                                          (st->cfg.flags & SLIDE_FLAG_TEST_PIPELINE_STALL) != 0, f32g,
+                                          clip && !st->trace[1]);
         if (e != cudaSuccess)
             return fail_cuda(e, "grad_reduce_adamw_cast launch");
         if (after_update && (e = cudaEventRecord(after_update, s)) != cudaSuccess)

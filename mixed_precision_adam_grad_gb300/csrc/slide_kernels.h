@@ -41,12 +41,16 @@ cudaError_t launch_grad_sqnorm(const ReplicaPtrs &g, int R, int64_t n, const Cli
 // Fused step.  When max_norm > 0 the kernel reduces the n_partials partial
 // sums (in a fixed order, identically in every block) to the clip coefficient.
 // status may be NULL; when check_finite is set and status is not NULL a
-// non-finite mean gradient sets bit 0 of *status.
+// non-finite mean gradient sets bit 0 of *status.  behind_prepass (clip only):
+// the last operation enqueued on `stream` is this step's clip pre-pass, so the
+// step is launched with programmatic serialisation and overlaps the
+// pre-pass's end; it reads the partials only after the pre-pass has ended.
 cudaError_t launch_grad_reduce_adamw_cast(const ReplicaPtrs &g, int R, int64_t n, float *theta,
                                           float *m, float *v, uint16_t *w, const AdamScalars &s,
                                           const ClipScratch *clip, int n_partials, float max_norm,
                                           bool check_finite, int device, cudaStream_t stream,
-                                          bool test_stall = false, bool f32_grads = false);
+                                          bool test_stall = false, bool f32_grads = false,
+                                          bool behind_prepass = false);
 
 // w[i] = bf16_rne(src[i]) (used when a caller overwrites a master copy).
 cudaError_t launch_cast_bf16(const float *src, uint16_t *w, int64_t n, cudaStream_t stream);

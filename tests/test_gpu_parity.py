@@ -173,6 +173,69 @@ def test_small_parity_fp32_grads(S, R, clip):
             assert r["not_bit_equal"] == 0, r
 
 
+@pytest.mark.parametrize("R,fp32", [(1, False), (4, False), (8, False), (3, True), (4, True)])
+def test_clipped_steps_back_to_back_overlapped_and_serialised(S, R, fp32):
+    """Clipped steps of three layers enqueued back to back on one stream, with
+    no host synchronisation between them.  A clipped step starts while its
+    pre-pass still runs (where a CTA of each fits on an SM together: BF16 with
+    R <= 4, FP32 with R <= 3) unless trace events sit between the two, as they
+    do for the second state here.  Both states must end with the same bits,
+    and with the oracle's result within the tolerance."""
+    sizes = [3 * (1 << 20) + 5, 2048 * 152 * 2 + 7, 4099]
+    steps = 4
+    w = W.Workload("b2b", [W.Unit(f"l{i}", [("flat", n)]) for i, n in enumerate(sizes)], R=R, steps=steps,
+                   seed=77, max_grad_norm=1e-3, lr=1e-3, fp32_grads=fp32)
+    hp = S.hparams(w.lr, w.beta1, w.beta2, w.eps, w.weight_decay, w.max_grad_norm)
+    flags = S.SLIDE_FLAG_FP32_GRADS if fp32 else 0
+    stream = torch.cuda.Stream()
+    # every step's replicas are generated up front, so nothing waits between steps
+    grads = {}
+    for t in range(1, steps + 1):
+        for li, n in enumerate(sizes):
+            grads[t, li] = [dev_grad_buf(n, fp32) for _ in range(R)]
+            for r in range(R):
+                pu.unit_grad_dev(w, li, t, r, grads[t, li][r].data_ptr())
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    for e in ev:
+        e.record(stream)
+    torch.cuda.synchronize()
+    overlapped = S.slide_state_create(sizes, R, flags=flags)
+    serialised = S.slide_state_create(sizes, R, flags=flags)
+    try:
+        th0 = [synth.master(n, w.seed, unit=li) for li, n in enumerate(sizes)]
+        for st in (overlapped, serialised):
+            for li in range(len(sizes)):
+                S.slide_layer_set(st, li, master=th0[li], step=0)
+        S.slide_trace_events(serialised, *ev)
+        for t in range(1, steps + 1):
+            for li in range(len(sizes)):
+                S.slide_layer_step(overlapped, li, grads[t, li], hp, stream)
+                S.slide_layer_step(serialised, li, grads[t, li], hp, stream)
+        torch.cuda.synchronize()
+        S.slide_trace_events(serialised)
+        hp_or = pu.hp_oracle(w)
+        for li, n in enumerate(sizes):
+            got = []
+            for st in (overlapped, serialised):
+                a, b, c = (np.empty(n, np.float32) for _ in range(3))
+                wb = np.empty(n, np.uint16)
+                assert S.slide_layer_get(st, li, a, b, c, wb) == steps
+                got.append((a, b, c, wb))
+            for x, y in zip(*got):
+                assert np.array_equal(x, y), f"layer {li}: overlapped and serialised steps differ"
+            th, m, v = th0[li].copy(), np.zeros(n, np.float32), np.zeros(n, np.float32)
+            wb = np.zeros(n, np.uint16)
+            for t in range(1, steps + 1):
+                oracle.layer_step([pu.unit_grad_host(w, li, t, r) for r in range(R)], th, m, v, wb, hp_or, t)
+            pu.assert_parity([pu.compare_fp32(f"theta l{li}", got[0][0], th),
+                              pu.compare_fp32(f"m l{li}", got[0][1], m),
+                              pu.compare_fp32(f"v l{li}", got[0][2], v),
+                              pu.compare_bf16(f"w l{li}", got[0][3], wb)])
+    finally:
+        S.slide_state_destroy(overlapped)
+        S.slide_state_destroy(serialised)
+
+
 def test_external_bf16_out_and_empty_layer(S):
     run_small(S, [0, 5, 4099], 2, clip=0.5, bf16_external=True)
 
