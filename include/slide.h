@@ -203,7 +203,10 @@ SLIDE_API slide_status slide_state_bytes(const slide_config *cfg, int64_t *devic
  *   bf16_out: device pointer receiving the BF16 copy, or NULL for the state's
  *     own copy (slide_layer_ptrs).  16-byte aligned.
  * Stream-ordered: returns before the GPU finishes.  Steps of one layer must be
- * ordered with each other (same stream, or synchronised by the caller).
+ * ordered with each other (same stream, or synchronised by the caller).  With
+ * the clip, the fused kernel is launched to overlap the end of the pre-pass
+ * (programmatic serialisation); it reads nothing the pre-pass writes before
+ * the pre-pass has ended, and both start only after the stream's earlier work.
  * Defined by: "SlideDP: Scaling Host-Resident LLM Fine-Tuning Across Multiple
  * GPUs", Core method (the R ranks' gradients of a layer reduced on the GPU;
  * one aggregated Adam update of the layer's FP32 master and moments per
@@ -353,8 +356,12 @@ SLIDE_API slide_status slide_layer_status(slide_state *st, int32_t layer);
 /* Tracing: CUDA events (cudaEvent_t values, created by the caller) that every
  * following slide_layer_step of this state records on its stream: before the
  * clip pre-pass, before the fused kernel and after it (any may be NULL; all
- * NULL turns tracing off).  Recording adds no synchronisation.  The caller may
- * pass fresh events before each step to time every launch separately.
+ * NULL turns tracing off).  The caller may pass fresh events before each step
+ * to time every launch separately.  Recording adds no host synchronisation,
+ * but with the clip on, an event before the fused kernel makes it wait for
+ * the pre-pass's end: without one the fused kernel starts while the pre-pass
+ * still runs (where a block of each fits on an SM together), so a traced
+ * clipped step can take longer than an untraced one.
  * Defined by: "SlideDP: Scaling Host-Resident LLM Fine-Tuning Across Multiple
  * GPUs", Reproduction (per-phase timing of the step with GPU events). */
 SLIDE_API slide_status slide_trace_events(slide_state *st, void *ev_prepass_start,
