@@ -701,6 +701,24 @@ def link_roofline_s(link, N, in_hbm):
                   26 * N / (link["bidir_gbs"] * G)))
 
 
+def e2e_link_roofline(e2e, link, n):
+    """The fastest the host link allows for one end-to-end step of n
+    parameters: the BF16 copy's device-to-host bytes run beside part of the
+    replicas' host-to-device bytes, at the rates measured with both directions
+    busy, and the rest of the larger direction runs alone (running the two
+    directions one after the other is slower on this link).  Returns the
+    bound in seconds and the measured step's fraction of it."""
+    G = 1e9
+    h2d, d2h = e2e["h2d_bytes_per_step"], e2e["d2h_bytes_per_step"]
+    ch, cd = link["h2d_concurrent_gbs"] * G, link["d2h_concurrent_gbs"] * G
+    t_both = min(h2d / ch, d2h / cd)             # both directions busy
+    t = t_both + (h2d - ch * t_both) / (link["h2d_gbs"] * G) + (d2h - cd * t_both) / (link["d2h_gbs"] * G)
+    measured = n / (e2e["value"] * G)
+    return {"s": t, "frac": t / measured,
+            "model": "device-to-host bytes beside host-to-device bytes at the concurrent rates, the rest alone; "
+                     "link rates from the run's probe"}
+
+
 def run_chunk_sweep(args, S, torch, synth, key, arena, link, points, steps=2):
     """TuneChunks-style sweep of the streamed engine's copy-in (host->device)
     and write-back (device->host) chunk sizes on one streamed workload: per
@@ -1082,6 +1100,8 @@ def run_ours(args):
     try:
         if streamed_keys:
             streamed = run_streamed(args, S, torch, synth, args.streamed_workload, arena)
+            if e2e is not None and "link" in streamed:
+                e2e["link_roofline"] = e2e_link_roofline(e2e, streamed["link"], n)
             also = streamed_keys[1:]
             if also:
                 streamed_also = {x: run_streamed(args, S, torch, synth, x, arena) for x in also}
@@ -1263,6 +1283,8 @@ def compact_headline(full):
                       "reasons": ck.get("reasons", []), "samples": ck.get("samples")}
     if full.get("e2e"):
         line["e2e"] = _pick(full["e2e"], ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step", "steps"))
+        if full["e2e"].get("link_roofline"):
+            line["e2e"]["link_frac"] = _r(full["e2e"]["link_roofline"]["frac"])
     for k in ("cpu_baseline", "cpu_baseline_all_cores"):
         c = full.get(k)
         if c:

@@ -237,3 +237,18 @@ def test_pinned_arena_carving():
         a.carve(1 << 21)
     a.reset()
     assert a.tensor(10, torch.uint8).data_ptr() == a.addr
+
+
+def test_e2e_link_roofline():
+    """The device-to-host bytes run beside part of the host-to-device bytes at
+    the concurrent rates; the rest of the host-to-device bytes run alone."""
+    link = {"h2d_gbs": 10.0, "d2h_gbs": 8.0, "h2d_concurrent_gbs": 5.0, "d2h_concurrent_gbs": 4.0}
+    e2e = {"h2d_bytes_per_step": 1000e9, "d2h_bytes_per_step": 100e9, "value": 1.0}
+    # 25 s with both busy (100 GB down at 4, 125 GB up at 5), then 875 GB up at 10
+    r = bench.e2e_link_roofline(e2e, link, n=112.5e9)
+    assert abs(r["s"] - 112.5) < 1e-9
+    assert abs(r["frac"] - 1.0) < 1e-12
+    # the smaller direction is host-to-device: it ends first and the rest goes down alone
+    e2e2 = {"h2d_bytes_per_step": 50e9, "d2h_bytes_per_step": 200e9, "value": 1.0}
+    r2 = bench.e2e_link_roofline(e2e2, link, n=30e9)
+    assert abs(r2["s"] - (10 + 160e9 / 8e9)) < 1e-9
