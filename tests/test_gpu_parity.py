@@ -107,6 +107,8 @@ def run_small(S, sizes, R, clip, steps=4, seed=11, flags=0, bf16_external=False,
                 if clip > 0 and n > 0:
                     gc = S.slide_layer_last_clip_coef(st, li)
                     assert abs(gc - coef) <= 2 * np.spacing(np.float32(coef)), (gc, coef)
+                if flags & S.SLIDE_FLAG_CHECK_FINITE:   # finite inputs: nothing may be flagged
+                    assert S.slide_layer_status(st, li) == S.SLIDE_OK
                 reports += rep
     finally:
         S.slide_state_destroy(st)
@@ -116,14 +118,14 @@ def run_small(S, sizes, R, clip, steps=4, seed=11, flags=0, bf16_external=False,
 SIZES = [1, 7, 8, 9, 1000, 1001, 4096 + 3, (1 << 20) + 5]
 
 
-@pytest.mark.parametrize("R", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_small_parity_no_clip_bit_exact(S, R):
     reps = run_small(S, SIZES, R, clip=0.0)
     for r in reps:
         assert r["not_bit_equal"] == 0, r
 
 
-@pytest.mark.parametrize("R", [1, 4, 8])
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("clip", [1e-3, 1e3])
 def test_small_parity_clip(S, R, clip):
     reps = run_small(S, [9, 4096 + 3, (1 << 20) + 5, 3 * (1 << 20) + 1], R, clip=clip)
@@ -162,7 +164,7 @@ def test_eps_regime_bit_exact(S, scale):
         S.slide_state_destroy(st)
 
 
-@pytest.mark.parametrize("R", [1, 3, 4, 8])
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("clip", [0.0, 1e-3])
 def test_small_parity_fp32_grads(S, R, clip):
     """FP32 gradient replicas (26 + 4R bytes per parameter): same arithmetic
@@ -234,6 +236,19 @@ def test_clipped_steps_back_to_back_overlapped_and_serialised(S, R, fp32):
     finally:
         S.slide_state_destroy(overlapped)
         S.slide_state_destroy(serialised)
+
+
+@pytest.mark.parametrize("R", [1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("clip", [0.0, 1e-3])
+@pytest.mark.parametrize("fp32", [False, True])
+def test_small_parity_with_finite_check(S, R, clip, fp32):
+    """The kernels with the non-finite check compiled in: on finite inputs the
+    same results as the oracle (bit for bit without the clip) and no flag."""
+    reps = run_small(S, [9, 4096 + 3, (1 << 20) + 5], R, clip=clip, steps=3, fp32=fp32,
+                     flags=S.SLIDE_FLAG_CHECK_FINITE)
+    if clip == 0.0:
+        for r in reps:
+            assert r["not_bit_equal"] == 0, r
 
 
 def test_external_bf16_out_and_empty_layer(S):
