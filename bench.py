@@ -701,6 +701,40 @@ def link_roofline_s(link, N, in_hbm):
                   26 * N / (link["bidir_gbs"] * G)))
 
 
+LINK_KEYS = ("h2d_gbs", "d2h_gbs", "h2d_concurrent_gbs", "d2h_concurrent_gbs", "bidir_gbs")
+
+
+def best_link(links):
+    """Per rate, the highest that the run's link probes measured (each
+    probe is a median of 20 copies).  That is the link's capability: the
+    host's pinned memory can slow down for a while (see the link monitors), so
+    a probe taken in a slow moment would lower the roofline of its leg and
+    raise that leg's fraction.  Rooflines computed from it are the tightest
+    the run supports."""
+    out = {k: max(x[k] for x in links) for k in LINK_KEYS}
+    out["probe"] = f"highest of the run's {len(links)} link probes, per rate"
+    return out
+
+
+def rebase_streamed(leg, link):
+    """Roofline and fractions of a streamed leg against `link` (the run's
+    best probe); the figures against the leg's own probe stay under
+    own_probe."""
+    N, in_hbm = leg["params"], leg["bf16_copy_in_hbm"]
+    t = link_roofline_s(link, N, in_hbm)
+    leg["own_probe"] = {"roofline_s": leg["roofline_s"], "frac": leg["frac"]}
+    leg["roofline_link"] = link
+    leg["roofline_s"], leg["frac"] = t, t / leg["s_per_step"]
+    leg["frac_fastest_step"] = t / leg["s_per_step_min"]
+    pp = leg.get("pipelined")
+    if pp:
+        per_dir, G = leg["link_bytes_per_step"]["h2d"], 1e9
+        tp = max(per_dir / (link["h2d_concurrent_gbs"] * G), per_dir / (link["d2h_concurrent_gbs"] * G),
+                 2 * per_dir / (link["bidir_gbs"] * G))
+        pp["roofline_s"] = tp
+        pp["frac"] = tp / pp["s_per_step"] if pp.get("s_per_step") else None
+
+
 def e2e_link_roofline(e2e, link, n):
     """The fastest the host link allows for one end-to-end step of n
     parameters: the BF16 copy's device-to-host bytes run beside part of the
@@ -1100,17 +1134,21 @@ def run_ours(args):
     try:
         if streamed_keys:
             streamed = run_streamed(args, S, torch, synth, args.streamed_workload, arena)
-            if e2e is not None and "link" in streamed:
-                e2e["link_roofline"] = e2e_link_roofline(e2e, streamed["link"], n)
             also = streamed_keys[1:]
             if also:
                 streamed_also = {x: run_streamed(args, S, torch, synth, x, arena) for x in also}
-            if args.chunk_sweep and arena is not None and "link" in streamed:
+            legs = [x for x in [streamed] + list((streamed_also or {}).values()) if "link" in x]
+            link = best_link([x["link"] for x in legs]) if legs else None
+            for leg in legs:
+                rebase_streamed(leg, link)
+            if e2e is not None and link:
+                e2e["link_roofline"] = e2e_link_roofline(e2e, link, n)
+            if args.chunk_sweep and arena is not None and link:
                 pts = [tuple(int(v) for v in p.split(":")) for p in args.chunk_sweep.split(",")]
                 chunk_sweep = {}
                 for key in [k for k in args.chunk_sweep_workloads.split(",") if k]:
                     if streamed_host_bytes(S, key, args) <= arena.nbytes:
-                        chunk_sweep[key] = run_chunk_sweep(args, S, torch, synth, key, arena, streamed["link"], pts)
+                        chunk_sweep[key] = run_chunk_sweep(args, S, torch, synth, key, arena, link, pts)
     finally:
         if arena is not None:
             arena.free()
@@ -1233,7 +1271,7 @@ def compact_streamed(leg):
         return {"skipped": leg["skipped"][:160]}
     spreads = sorted(p["unit_max_over_median"] for p in leg.get("per_step", [])
                      if p.get("unit_max_over_median") is not None)
-    link = leg.get("link", {})
+    link = leg.get("roofline_link", leg.get("link", {}))
     out = {"bf16_in_hbm": leg["bf16_copy_in_hbm"], "s_per_step": _r(leg["s_per_step"]),
            "roofline_s": _r(leg["roofline_s"]), "frac": _r(leg["frac"]),
            "frac_fastest": _r(leg["frac_fastest_step"]),

@@ -252,3 +252,23 @@ def test_e2e_link_roofline():
     e2e2 = {"h2d_bytes_per_step": 50e9, "d2h_bytes_per_step": 200e9, "value": 1.0}
     r2 = bench.e2e_link_roofline(e2e2, link, n=30e9)
     assert abs(r2["s"] - (10 + 160e9 / 8e9)) < 1e-9
+
+
+def test_streamed_legs_use_the_runs_best_link_probe():
+    """A leg whose own probe caught the link in a slow moment is measured
+    against the best probe of the run, never against a lowered roofline."""
+    fast = {"h2d_gbs": 210.0, "d2h_gbs": 190.0, "h2d_concurrent_gbs": 170.0, "d2h_concurrent_gbs": 170.0,
+            "bidir_gbs": 340.0}
+    slow = {k: v * 0.8 for k, v in fast.items()}
+    best = bench.best_link([slow, fast])
+    assert all(best[k] == fast[k] for k in bench.LINK_KEYS)
+    N = 1_000_000_000
+    t_slow = bench.link_roofline_s(slow, N, True)
+    leg = {"params": N, "bf16_copy_in_hbm": True, "s_per_step": t_slow, "s_per_step_min": t_slow,
+           "roofline_s": t_slow, "frac": 1.0, "link_bytes_per_step": {"h2d": 12 * N, "d2h": 12 * N},
+           "pipelined": {"s_per_step": t_slow}}
+    bench.rebase_streamed(leg, best)
+    assert leg["own_probe"]["frac"] == 1.0
+    assert abs(leg["frac"] - 0.8) < 1e-12          # every rate 1.25x faster: the bound is 0.8x the time
+    assert abs(leg["pipelined"]["frac"] - 0.8) < 1e-12
+    assert leg["roofline_link"] is best
