@@ -350,6 +350,13 @@ __device__ __forceinline__ uint64_t make_evict_first()
 __device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void wait_prerequisites() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// Shared memory of one SM on sm_103a, and what a CTA takes beyond its
+// dynamic shared memory (its static shared memory and the per-CTA
+// reservation), rounded up: two CTAs fit on an SM together when their
+// dynamic sizes plus this margin stay within the SM's.
+constexpr int64_t kSmemPerSm = 228 * 1024;
+constexpr int64_t kCoResidentMargin = 4096;
+
 template <typename G, int R>
 struct Pipe {
     static constexpr uint32_t kGradBytes = kTile * sizeof(G);
@@ -583,9 +590,11 @@ struct SqArgs {
 // accumulate the squared replica means.  The loads in flight sit in shared
 // memory, not in registers.  Tile and ring sizes were chosen by timing the
 // whole clipped step: 4 KiB tiles in 8 stages beat 8 KiB tiles, 4, 6 or 12
-// stages, and the register-path kernel this replaced.  The part after the
-// last whole tile is read with plain vector loads by one CTA.  Each block
-// writes one double partial, in a fixed order.
+// stages, and the register-path kernel this replaced.  With five or more BF16
+// replicas (four or more FP32), the ring is cut to what leaves room for a CTA
+// of the clipped step on the SM, down to 3 stages (see SqPipe::kBeside).  The
+// part after the last whole tile is read with plain vector loads by one CTA.
+// Each block writes one double partial, in a fixed order.
 template <typename G, int R>
 struct SqPipe {
     static constexpr uint32_t kGradBytes = 4096;                 // per replica per tile
@@ -593,7 +602,13 @@ struct SqPipe {
     static constexpr int kPer = (int)(16 / sizeof(G));           // parameters per 16-byte vector
     static constexpr uint32_t kStageBytes = R * kGradBytes;
     static constexpr int kFit = (int)((192u * 1024u) / kStageBytes);
-    static constexpr int kStages = kFit > 8 ? 8 : (kFit < 2 ? 2 : kFit);
+    static constexpr int kAlone = kFit > 8 ? 8 : (kFit < 2 ? 2 : kFit);
+    // Stages that leave room on the SM for one CTA of the clipped step beside
+    // this one, so that the step can start while this pass runs.  Where at
+    // least 3 fit (at least 72 KiB in flight per SM), the ring takes no more.
+    static constexpr int64_t kBeside =
+        (kSmemPerSm - (int64_t)Pipe<G, R>::kSmemBytes - kCoResidentMargin) / (int64_t)(kStageBytes + 16);
+    static constexpr int kStages = kBeside >= 3 && kBeside < kAlone ? (int)kBeside : kAlone;
     static constexpr uint32_t kSmemBytes = kStages * kStageBytes + 2 * kStages * 8;
     static constexpr int kVec = (int)(kGradBytes / (16 * kConsumerWarps * 32));  // vectors per thread per replica
     static_assert(kVec >= 1 && kGradBytes == (uint32_t)kVec * 16 * kConsumerWarps * 32,
@@ -793,7 +808,7 @@ bool fits_beside_prepass(int device, uint32_t step_smem, uint32_t prepass_smem)
         if (device >= 0 && device < kMaxDevices)
             cache[device].store(per_sm, std::memory_order_relaxed);
     }
-    return (int64_t)step_smem + prepass_smem + 4096 <= per_sm;
+    return (int64_t)step_smem + prepass_smem + kCoResidentMargin <= per_sm;
 }
 
 // Raise the fused kernel's dynamic shared-memory limit on `device` (once per

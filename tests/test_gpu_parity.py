@@ -175,14 +175,14 @@ def test_small_parity_fp32_grads(S, R, clip):
             assert r["not_bit_equal"] == 0, r
 
 
-@pytest.mark.parametrize("R,fp32", [(1, False), (4, False), (8, False), (3, True), (4, True)])
+@pytest.mark.parametrize("R,fp32", [(1, False), (4, False), (8, False), (3, True), (6, True), (8, True)])
 def test_clipped_steps_back_to_back_overlapped_and_serialised(S, R, fp32):
     """Clipped steps of three layers enqueued back to back on one stream, with
     no host synchronisation between them.  A clipped step starts while its
-    pre-pass still runs (where a CTA of each fits on an SM together: BF16 with
-    R <= 4, FP32 with R <= 3) unless trace events sit between the two, as they
-    do for the second state here.  Both states must end with the same bits,
-    and with the oracle's result within the tolerance."""
+    pre-pass still runs (where a CTA of each fits on an SM together: BF16
+    replicas, and FP32 replicas up to R = 6) unless trace events sit between
+    the two, as they do for the second state here.  Both states must end with
+    the same bits, and with the oracle's result within the tolerance."""
     sizes = [3 * (1 << 20) + 5, 2048 * 152 * 2 + 7, 4099]
     steps = 4
     w = W.Workload("b2b", [W.Unit(f"l{i}", [("flat", n)]) for i, n in enumerate(sizes)], R=R, steps=steps,
