@@ -585,8 +585,9 @@ struct SqArgs {
 
 // Clip pre-pass as a bulk-copy pipeline, the fused kernel's structure for a
 // read-only pass: one CTA per SM; a producer lane streams tiles of 4 KiB per
-// replica (2048 BF16 or 1024 FP32 parameters) into a ring of up to 8 stages
-// (at most 192 KiB), and 8 consumer warps read them from shared memory and
+// replica (2048 BF16 or 1024 FP32 parameters; larger with fewer than four
+// replicas, see SqPipe::kGradBytes) into a ring of up to 8 stages (at most
+// 192 KiB), and 8 consumer warps read them from shared memory and
 // accumulate the squared replica means.  The loads in flight sit in shared
 // memory, not in registers.  Tile and ring sizes were chosen by timing the
 // whole clipped step: 4 KiB tiles in 8 stages beat 8 KiB tiles, 4, 6 or 12
@@ -597,7 +598,13 @@ struct SqArgs {
 // Each block writes one double partial, in a fixed order.
 template <typename G, int R>
 struct SqPipe {
-    static constexpr uint32_t kGradBytes = 4096;                 // per replica per tile
+    // Bytes per replica per tile: 4 KiB from four replicas on; with fewer, a
+    // tile holds more parameters (16 KiB at R = 1, 8 KiB at R = 2 and 3), so
+    // that the fixed cost of a tile (a copy issued, a barrier waited on and
+    // released) is spread over enough work: with 4 KiB tiles one replica's
+    // pass ran at 0.41 of the copy peak and the whole clipped step at 0.906,
+    // with 16 KiB at 0.57 and 0.941.
+    static constexpr uint32_t kGradBytes = R >= 4 ? 4096u : (R == 1 ? 16384u : 8192u);
     static constexpr int kTile = (int)(kGradBytes / sizeof(G));  // parameters per tile
     static constexpr int kPer = (int)(16 / sizeof(G));           // parameters per 16-byte vector
     static constexpr uint32_t kStageBytes = R * kGradBytes;
